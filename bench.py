@@ -1,0 +1,487 @@
+"""Benchmark of the SP-region hot path on GB300.
+
+One step = one pass of the whole hot path over one synthetic batch of the
+pages' benchmark shape (T=2, S=2048, B=2, H=768, bf16, RMSNorm, p=0.1):
+  forward of every sequence shard (reduce-scatter's reduce, dropout, residual,
+  RMSNorm) -> sp2hp of the norm output -> hp2sp back -> backward of every
+  shard (norm, residual and dropout backward, dgamma).
+Each step is one CUDA graph replay; inputs rotate over buffer sets whose
+total is more than twice the L2 size, so HBM (not L2) serves them.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Rank 0 prints one JSON line.  Under torchrun every rank runs the same
+workload on its own GPU (weak scaling; no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "pages_rms_bf16"
+METRIC = "SP-region fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+LAUNCHES_PER_STEP = 5  # fwd, sp2hp, hp2sp, bwd, dgamma column sum
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--roofline-iters", type=int, default=400)
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what each launch must move at minimum)
+# ---------------------------------------------------------------------------
+
+def fwd_bytes(w, rows):
+    e = 2 if w.dtype == "bf16" else 4
+    per_elem = w.T * e + e + e + e + (1 if w.p > 0 else 0)  # partials, residual, h, y, mask
+    per_row = 4 + (4 if w.norm == "ln" else 0)               # rstd (+ mean)
+    return rows * (w.H * per_elem + per_row) + w.H * e * (2 if w.norm == "ln" else 1)
+
+
+def bwd_bytes(w, rows):
+    e = 2 if w.dtype == "bf16" else 4
+    per_elem = 5 * e + (1 if w.p > 0 else 0)  # dy, dh_out, h, d_residual, d_sum (+ mask)
+    per_row = 4 + (4 if w.norm == "ln" else 0)
+    return rows * (w.H * per_elem + per_row) + w.H * (e + 4 * (2 if w.norm == "ln" else 1))
+
+
+def layout_bytes(w, rows):
+    e = 2 if w.dtype == "bf16" else 4
+    return 2 * rows * w.H * e
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index, enabled=True):
+        self.proc = None
+        self.idx = device_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        if enabled:
+            try:
+                os.makedirs(os.path.dirname(self.path), exist_ok=True)
+                self.f = open(self.path, "w")
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                    stderr=subprocess.DEVNULL)
+            except (OSError, FileNotFoundError):
+                self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smmax=float(parts[2]),
+                                 power=float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smmax"] for r in rows), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from residual_sp_rs_gb300 import build as spbuild
+    from residual_sp_rs_gb300 import ops, synthetic as syn
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        spbuild.build()
+    if world > 1:
+        dist.barrier()
+    ops.lib()
+
+    w = syn.WORKLOADS[args.workload]
+    T, H = w.T, w.H
+    rows = w.S * w.B
+    tdt = syn.torch_dtype(w.dtype)
+    desc = ops.make_desc(T, 0, w.S, w.B, H, w.dtype, w.norm, w.p, w.eps, w.seed, nshards=T)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def make_set(k):
+        inp = syn.fwd_inputs(w, dev, seed=w.input_seed + 17 * k)
+        gr = syn.upstream_grads(w, dev, seed=w.input_seed + 17 * k)
+        s = dict(partials=inp["partials"], residual=inp["residual"].view(rows, H),
+                 gamma=inp["gamma"], beta=inp["beta"], dy=gr["dy"].view(rows, H),
+                 dh=gr["dh_out"].view(rows, H))
+        s["h"] = torch.empty((rows, H), device=dev, dtype=tdt)
+        s["y"] = torch.empty((rows, H), device=dev, dtype=tdt)
+        s["mask"] = torch.empty((rows, H), device=dev, dtype=torch.uint8) if w.p > 0 else None
+        s["rstd"] = torch.empty(rows, device=dev)
+        s["mean"] = torch.empty(rows, device=dev) if w.norm == "ln" else None
+        s["y_hp"] = torch.empty((T, rows, H // T), device=dev, dtype=tdt)
+        s["y_sp"] = torch.empty((rows, H), device=dev, dtype=tdt)
+        s["d_res"] = torch.empty((rows, H), device=dev, dtype=tdt)
+        s["d_sum"] = torch.empty((rows, H), device=dev, dtype=tdt)
+        s["dgamma"] = torch.empty(H, device=dev)
+        s["dbeta"] = torch.empty(H, device=dev) if w.norm == "ln" else None
+        s["ws"] = ops.workspace_for(desc, dev)
+        return s
+
+    def set_bytes(s):
+        return sum(v.numel() * v.element_size() for k, v in s.items()
+                   if isinstance(v, torch.Tensor)) + sum(p.numel() * p.element_size()
+                                                         for p in s["partials"])
+
+    first = make_set(0)
+    per_set = set_bytes(first)
+    n_sets = max(2, -(-2 * l2 // per_set) + 1)
+    sets = [first] + [make_set(k) for k in range(1, n_sets)]
+
+    def fwd(s, stream=None):
+        ops.sp_rs_dropout_residual_norm_fwd(desc, s["partials"], s["residual"], s["gamma"], s["beta"],
+                                            s["h"], s["y"], s["mask"], s["rstd"], s["mean"], stream)
+
+    def bwd(s, stream=None):
+        ops.sp_rs_dropout_residual_norm_bwd(desc, s["dy"], s["dh"], s["h"], s["gamma"], s["mask"],
+                                            s["rstd"], s["mean"], s["d_res"], s["d_sum"], s["dgamma"],
+                                            s["dbeta"], s["ws"], stream=stream)
+
+    def step(s):
+        fwd(s)
+        ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype)
+        ops.hp2sp(s["y_hp"], s["y_sp"], rows, H, T, w.dtype)
+        bwd(s)
+
+    # one CUDA graph per buffer set, each one full step
+    for s in sets:
+        step(s)
+    torch.cuda.synchronize()
+    graphs = []
+    cap_stream = torch.cuda.Stream()
+    for s in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="relaxed"):
+            step(s)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        graphs[i % n_sets].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region ----------------------------------------------------------
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.2)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for i in range(args.steps):
+        graphs[i % n_sets].replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    tokens = rows * args.steps * world
+    value = tokens / (ms / 1e3)
+    step_bytes = fwd_bytes(w, rows) + bwd_bytes(w, rows) + 2 * layout_bytes(w, rows)
+    step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
+
+    # ---- per-launch durations of the main kernels (events on the launch stream)
+    def time_launches(fn, iters):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        for i in range(iters):
+            s = sets[i % n_sets]
+            evs[i][0].record()
+            fn(s)
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / iters
+
+    for s in sets:
+        fwd(s)
+        bwd(s)
+    torch.cuda.synchronize()
+    t_fwd = time_launches(fwd, args.roofline_iters)
+    t_bwd = time_launches(bwd, args.roofline_iters)
+    t_sp2hp = time_launches(lambda s: ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype),
+                            args.roofline_iters)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    kern = {"fwd": (t_fwd, fwd_bytes(w, rows), "sp_fwd_kernel"),
+            "bwd": (t_bwd, bwd_bytes(w, rows), "sp_bwd_kernel+sp_colsum_kernel"),
+            "sp2hp": (t_sp2hp, layout_bytes(w, rows), "sp_layout_kernel")}
+    dom = max(("fwd", "bwd"), key=lambda k: kern[k][0])
+    d_ms, d_bytes, d_name = kern[dom]
+    achieved = d_bytes / (d_ms / 1e3) / 1e9
+    traffic = None
+    try:
+        tr = json.load(open(os.path.join(ROOT, "profiles", f"{dom}_{args.workload}_traffic.json")))
+        from residual_sp_rs_gb300.build import _deps
+        import hashlib
+        h = hashlib.sha256()
+        for p in sorted(_deps()):
+            h.update(open(p, "rb").read())
+        if tr.get("source_sha256") == h.hexdigest():
+            traffic = tr.get("bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": traffic, "kernel": d_name,
+                "peak_source": peak_src, "algorithmic_bytes_per_launch": d_bytes,
+                "launch_ms": round(d_ms, 5),
+                "per_kernel": {k: {"launch_ms": round(v[0], 5), "algorithmic_bytes": v[1],
+                                   "gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
+                                   "frac_of_measured": round(v[1] / (v[0] / 1e3) / 1e9 / hbm_peak, 4)}
+                               for k, v in kern.items()}}
+
+    # ---- end to end: pinned host inputs in, results out, every step -------------
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, desc, dev, sets[0], rows, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if w.dtype == "bf16" else "f32", "data": "synthetic (seeded torch.Generator)",
+            "config": {"workload": f"{w.name}: SP region fwd+sp2hp+hp2sp+bwd, T={T} S={w.S} B={w.B} "
+                                   f"H={H} {w.dtype} {w.norm} p={w.p}",
+                       "T": T, "S": w.S, "B": w.B, "H": H, "norm": w.norm, "p": w.p,
+                       "tokens_per_step": rows, "parallelism": f"replica x{world}",
+                       "l2": f"inputs rotate over {n_sets} buffer sets, {n_sets * per_set / 1e6:.0f} MB "
+                             f"> 2x L2 ({l2 / 1e6:.0f} MB)",
+                       "launch": "one CUDA graph replay per step, programmatic dependent launch"},
+            "hbm_gbs_step": round(step_gbs, 1),
+            "hbm_frac_step": round(step_gbs / hbm_peak, 4),
+            "roofline": roofline,
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, desc, dev, s, rows, world):
+    """Through the public API with HOST buffers: every step copies its inputs
+    from pinned host memory, runs the step and reads the results back."""
+    import torch
+
+    from residual_sp_rs_gb300 import ops
+
+    T, H = w.T, w.H
+    host_in = {k: s[k].cpu().pin_memory() for k in ("residual", "dy", "dh", "gamma")}
+    host_parts = [p.view(rows, H).cpu().pin_memory() for p in s["partials"]]
+    outs = ("y", "d_res", "d_sum", "dgamma")
+    host_out = {k: torch.empty(s[k].shape, dtype=s[k].dtype, pin_memory=True) for k in outs}
+    bi = sum(v.numel() * v.element_size() for v in host_in.values()) + \
+        sum(v.numel() * v.element_size() for v in host_parts)
+    bo = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one_step():
+        for k, v in host_in.items():
+            s[k].copy_(v, non_blocking=True)
+        for p, hp in zip(s["partials"], host_parts):
+            p.view(rows, H).copy_(hp, non_blocking=True)
+        ops.sp_rs_dropout_residual_norm_fwd(desc, s["partials"], s["residual"], s["gamma"], s["beta"],
+                                            s["h"], s["y"], s["mask"], s["rstd"], s["mean"])
+        ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype)
+        ops.hp2sp(s["y_hp"], s["y_sp"], rows, H, T, w.dtype)
+        ops.sp_rs_dropout_residual_norm_bwd(desc, s["dy"], s["dh"], s["h"], s["gamma"], s["mask"],
+                                            s["rstd"], s["mean"], s["d_res"], s["d_sum"], s["dgamma"],
+                                            s["dbeta"], s["ws"])
+        for k in outs:
+            host_out[k].copy_(s[k], non_blocking=True)
+
+    for _ in range(5):
+        one_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.e2e_steps):
+        one_step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    return {"value": round(rows * args.e2e_steps * world / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps,
+            "ms_per_step": round(ms / args.e2e_steps, 5)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: the cpu_baseline leg and the reference arm
+# ---------------------------------------------------------------------------
+
+def _oracle_setup(w):
+    import oracle
+    from residual_sp_rs_gb300 import synthetic as syn
+
+    oracle.build()
+    inp = syn.fwd_inputs(w, "cpu")
+    gr = syn.upstream_grads(w, "cpu")
+    H, rows = w.H, w.S * w.B
+    st = dict(parts=[syn.to_storage(p).reshape(rows, H) for p in inp["partials"]],
+              res=syn.to_storage(inp["residual"]).reshape(rows, H),
+              gamma=syn.to_storage(inp["gamma"]),
+              beta=None if inp["beta"] is None else syn.to_storage(inp["beta"]),
+              dy=syn.to_storage(gr["dy"]).reshape(rows, H),
+              dh=syn.to_storage(gr["dh_out"]).reshape(rows, H))
+    return oracle, st
+
+
+def _oracle_step(oracle, w, st, row0, n):
+    """The oracle's pass over token rows [row0, row0+n) (n a multiple of T):
+    forward, sp2hp/hp2sp of the norm output, backward."""
+    pr = oracle.problem(w.T, 0, w.S, w.B, w.H, w.dtype, w.norm, float(np.float32(w.p)),
+                        float(np.float32(w.eps)), w.seed)
+    grows = np.arange(row0, row0 + n)
+    f = oracle.fwd_rows(pr, grows, [p[row0:row0 + n] for p in st["parts"]], st["res"][row0:row0 + n],
+                        st["gamma"], st["beta"], w.dtype)
+    hp = oracle.sp2hp(f["y"], w.T)
+    oracle.hp2sp(hp)
+    oracle.bwd_rows(pr, st["dy"][row0:row0 + n], st["dh"][row0:row0 + n], f["h"], st["gamma"],
+                    f["mask"], w.dtype)
+
+
+def cpu_baseline(w, seconds):
+    oracle, st = _oracle_setup(w)
+    rows = w.S * w.B
+    n = max(w.T, (64 // w.T) * w.T)
+    done, t0 = 0, time.perf_counter()
+    row0 = 0
+    while time.perf_counter() - t0 < seconds:
+        _oracle_step(oracle, w, st, row0, n)
+        done += n
+        row0 = (row0 + n) % (rows - n + 1)
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} token rows ({done / rows:.2f} of one step's {rows}) of the same "
+                      f"workload through the fp64 oracle (fwd, sp2hp, hp2sp, bwd), {dt:.1f} s, "
+                      f"single thread; host has {os.cpu_count()} cores"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from residual_sp_rs_gb300 import synthetic as syn
+
+    w = syn.WORKLOADS[args.workload]
+    oracle, st = _oracle_setup(w)
+    rows = w.S * w.B
+    # size each step's sample so the whole run ends within about two minutes
+    t0 = time.perf_counter()
+    _oracle_step(oracle, w, st, 0, w.T * 4)
+    per_row = (time.perf_counter() - t0) / (w.T * 4)
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    n = int(budget / per_row) // w.T * w.T
+    n = max(w.T, min(n, rows))
+    for i in range(args.warmup):
+        _oracle_step(oracle, w, st, (i * n) % (rows - n + 1), n)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_step(oracle, w, st, (i * n) % (rows - n + 1), n)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    sample = (f"{n} of {rows} token rows per step through the fp64 oracle "
+              f"(fwd, sp2hp, hp2sp, bwd), single thread; host has {os.cpu_count()} cores")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: SP region fwd+sp2hp+hp2sp+bwd, T={w.T} S={w.S} "
+                                   f"B={w.B} H={w.H} {w.dtype} {w.norm} p={w.p}",
+                       "tokens_per_step_sampled": n},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

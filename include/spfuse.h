@@ -1,0 +1,179 @@
+/*
+ * spfuse.h -- C ABI of libspfuse, the sequence-parallel (SP) region hot path
+ * on one GB300 (sm_103a).
+ *
+ * The SP region is the per-token work between two tensor-parallel (TP)
+ * regions: the reduce half of a reduce-scatter over the T row-parallel
+ * partial outputs, dropout, the residual add and the next sub-layer's norm,
+ * plus the backward of that chain and the sp2hp / hp2sp layout transforms.
+ *
+ * Sources (the pages this library follows):
+ *  [MT3] MiniMind-tron ch.3 "Sequence Parallelism: layout and gradients"
+ *  [MT4] MiniMind-tron ch.4 "Sequence Parallelism: memory bounds, async
+ *        communication and recompute"
+ *  [SPN] "Sequence Parallel" notes (cloudchewie), distributed training /
+ *        parallelism
+ *  [ATL] LLM Infra Atlas "03 · Sequence Parallelism: AG/RS replacing
+ *        all-reduce"
+ *
+ * General conventions
+ *  - Memory: every pointer argument is a DEVICE pointer (except the `partials`
+ *    array itself, which is a host array of device pointers).  The caller owns
+ *    all memory; the library never allocates, frees or synchronises.
+ *  - Execution: every call enqueues its kernels on `stream` and returns
+ *    without waiting.  Kernels are launched with programmatic dependent
+ *    launch enabled; each kernel waits for the preceding work in the stream
+ *    before it reads any input, so stream order is preserved.
+ *  - Layout: activations are [S, B, H] row-major with the sequence as dim 0
+ *    ([MT3] §3.2.4, [ATL] §3).  Sequence shard j of T is the contiguous row
+ *    range [j*R, (j+1)*R) of the [S*B, H] view, R = (S/T)*B.
+ *  - Validation: all arguments are checked before anything is launched; on
+ *    error nothing is launched and the status says why.  A CUDA error at
+ *    launch is reported as SP_ERR_CUDA.
+ *  - Outputs must not alias inputs.  The library keeps no state between calls
+ *    and is safe to call from several host threads.
+ */
+#ifndef SPFUSE_H
+#define SPFUSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sp_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  SP_OK = 0,
+  SP_ERR_INVALID_ARG = 1,     /* null pointer, bad p / eps / T / j */
+  SP_ERR_SHAPE = 2,           /* S % T != 0, H not a multiple of the vector width, H too large */
+  SP_ERR_ALIGN = 3,           /* a pointer is not aligned as required */
+  SP_ERR_DTYPE = 4,           /* unknown dtype or norm */
+  SP_ERR_WORKSPACE = 5,       /* workspace missing or smaller than required */
+  SP_ERR_CUDA = 6,            /* a CUDA runtime call failed */
+  SP_ERR_NOT_IMPLEMENTED = 7
+} sp_status_t;
+
+typedef enum { SP_F32 = 0, SP_BF16 = 1 } sp_dtype_t;
+typedef enum { SP_RMSNORM = 0, SP_LAYERNORM = 1 } sp_norm_t;
+
+/* Problem statement of one SP region ([MT3] §3.2.1, §3.2.4; [SPN] LayerNorm
+ * formula).  Requirements: 1 <= T <= 8; 0 <= j < T; j + nshards <= T;
+ * S >= 0, B >= 0, S % T == 0; H > 0 and H % 8 == 0 (bf16) or H % 4 == 0
+ * (f32); H <= 16384 (bf16) or 8192 (f32), the longest row the row kernels
+ * keep in registers; S*B*H < 2^46; 0 <= p < 1; eps > 0 and finite. */
+typedef struct sp_rs_desc_t {
+  int32_t T;        /* TP group size = SP group size ([MT3] §3.2.4) */
+  int32_t j;        /* first sequence shard processed by this call */
+  int64_t S;        /* full sequence length */
+  int64_t B;        /* micro-batch */
+  int64_t H;        /* hidden size */
+  int32_t dtype;    /* sp_dtype_t: activation dtype of every tensor argument */
+  int32_t norm;     /* sp_norm_t */
+  float p;          /* dropout probability */
+  float eps;        /* norm epsilon */
+  uint64_t seed;    /* Philox4x32-10 key of the dropout mask */
+  int32_t nshards;  /* shards j .. j+nshards-1 in one call; 0 is read as 1 */
+  int32_t reserved; /* must be 0 */
+} sp_rs_desc_t;
+
+/* Forward of the SP region for sequence shards j .. j+nshards-1.
+ *
+ *   Y[r,c]  = sum_{t=0}^{T-1} P_t[row j*R + r, c]      reduce half of the
+ *             reduce-scatter, fp32, rank order ([MT3] §3.2.1, §3.3.3)
+ *   M[r,c]  = Philox4x32-10(key = seed, counter = (g>>2, 0)) word g&3 >= floor(p*2^32),
+ *             g = (j*R + r)*H + c  (global element index; 1-byte mask,
+ *             [SPN] MLP activation size)
+ *   h[r,c]  = residual[r,c] + Y[r,c]*M[r,c]/(1-p)     dropout then residual
+ *             add ([MT3] §3.5; [ATL] §1), stored rounded to dtype
+ *   y[r,:]  = RMSNorm: gamma * h * rstd, rstd = 1/sqrt(mean(h^2) + eps)
+ *             ([MT4] §4.2.1.1, fp32 inside, one rounding at the end)
+ *             LayerNorm: gamma * (h - mean) * rstd + beta,
+ *             rstd = 1/sqrt(var + eps), population variance ([SPN] formula)
+ *             computed from the stored h.
+ *
+ * partials : host array of T device pointers, each a full [S,B,H] tensor
+ *            (16-byte aligned).  Only rows of the processed shards are read.
+ * residual : [nshards*R, H] residual stream of those shards.
+ * gamma    : [H]; beta: [H] for LayerNorm (ignored for RMSNorm).
+ * h_out, y_out : [nshards*R, H] outputs (residual stream, norm output).
+ * mask_out : [nshards*R, H] bytes (0/1); may be NULL only when p == 0.
+ * rstd_out : [nshards*R] fp32.  mean_out: [nshards*R] fp32, LayerNorm only
+ *            (ignored for RMSNorm).
+ * Alignment: activation pointers and mask 16 bytes; rstd/mean 4 bytes.
+ * With no rows to process (S == 0 or B == 0) the call returns SP_OK at once
+ * and no pointer is checked or touched. */
+sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc,
+                                            const void* const* partials,
+                                            const void* residual,
+                                            const void* gamma, const void* beta,
+                                            void* h_out, void* y_out,
+                                            uint8_t* mask_out,
+                                            float* rstd_out, float* mean_out,
+                                            sp_stream_t stream);
+
+/* Bytes of device workspace sp_rs_dropout_residual_norm_bwd needs for this
+ * problem on the CURRENT device (it depends on the SM count).  Returns 0 for
+ * an invalid descriptor. */
+size_t sp_rs_bwd_workspace_bytes(const sp_rs_desc_t* desc);
+
+/* Backward of the SP region for shards j .. j+nshards-1.
+ *
+ *   g      = gamma * dy
+ *   RMS:   xhat = h*rstd,          dh = rstd*(g - xhat*mean(g*xhat))
+ *   LN:    xhat = (h-mean)*rstd,   dh = rstd*(g - mean(g) - xhat*mean(g*xhat))
+ *   dH     = dh + dh_out                                (dh_out may be NULL)
+ *   d_residual = dH                    (the residual add passes dH on)
+ *   d_sum  = dH * M / (1-p)            (dropout backward needs only M,
+ *                                       [SPN] MLP activation size)
+ *   d_sum is the gradient of the reduced sum and so of each partial P_t on
+ *   these rows: the all-gather of the backward followed by the add node's
+ *   copy ([MT3] §3.3.3.1) needs no T copies on one GPU.
+ *   dgamma[c] = sum_r dy[r,c]*xhat[r,c];  dbeta[c] = sum_r dy[r,c]
+ *   over the processed rows only: the sum over shards is the all-reduce of
+ *   replicated-parameter gradients ([MT3] §3.4.2.1), which a call with
+ *   nshards = T performs in place.  Deterministic two-pass reduction.
+ *
+ * dy, dh_out, h_saved : [nshards*R, H]; gamma: [H]; mask: [nshards*R, H]
+ * bytes (NULL iff p == 0); rstd, mean: [nshards*R] as written by the forward
+ * (mean ignored for RMSNorm).  d_residual, d_sum: [nshards*R, H] outputs;
+ * dgamma, dbeta: [H] fp32 outputs (dbeta ignored for RMSNorm).
+ * workspace: device scratch of at least sp_rs_bwd_workspace_bytes(desc)
+ * bytes, 16-byte aligned; its contents need no initialisation and are
+ * meaningless afterwards.  With no rows to process only dgamma (and dbeta)
+ * are required; they are set to zero. */
+sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc,
+                                            const void* dy, const void* dh_out,
+                                            const void* h_saved, const void* gamma,
+                                            const uint8_t* mask,
+                                            const float* rstd, const float* mean,
+                                            void* d_residual, void* d_sum,
+                                            float* dgamma, float* dbeta,
+                                            void* workspace, size_t workspace_bytes,
+                                            sp_stream_t stream);
+
+/* sp2hp ([ATL] §5): sequence-split -> hidden-split.  `in` is [N, H]: the T
+ * rank shards [N/T, H] stacked in rank order; `out` is [T][N][H/T] where
+ * out[r] is what rank r holds after the all-to-all:
+ *   out[r][n][c] = in[n][r*H/T + c].
+ * Requirements: N % T == 0, (H/T) % 8 == 0 (bf16) or % 4 == 0 (f32),
+ * 1 <= T <= 8, both pointers 16-byte aligned.  Bit-exact copy. */
+sp_status_t sp2hp(const void* in, void* out, int64_t N, int64_t H, int32_t T,
+                  int32_t dtype, sp_stream_t stream);
+
+/* hp2sp ([ATL] §5): the inverse, out[n][r*H/T + c] = in[r][n][c]. */
+sp_status_t hp2sp(const void* in, void* out, int64_t N, int64_t H, int32_t T,
+                  int32_t dtype, sp_stream_t stream);
+
+/* Static string for a status code. */
+const char* sp_status_string(sp_status_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t sp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPFUSE_H */

@@ -1,0 +1,297 @@
+// api.cu -- the C ABI of libspfuse: argument validation, kernel-shape
+// selection and launches.  Declarations and the contract of every entry
+// point are in include/spfuse.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+
+#include "../../include/spfuse.h"
+#include "launch.h"
+
+namespace spf {
+namespace {
+
+constexpr int kMaxFwdTPR = 512;
+constexpr int kMaxVPT = 4;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int elem_bytes(int dtype) { return dtype == SP_BF16 ? 2 : 4; }
+
+// Test hook: when SPFUSE_FAIL_LAUNCH is set in the environment, every launch
+// reports a CUDA failure without touching the GPU, so error propagation can be
+// exercised on a machine with or without a device.
+bool inject_launch_failure() {
+  static const bool on = std::getenv("SPFUSE_FAIL_LAUNCH") != nullptr;
+  return on;
+}
+
+struct Problem {
+  int T, j, nshards, dtype, norm;
+  int64_t S, B, H, R, rows;
+  int ev, nvec;
+};
+
+// Checks the descriptor (not the pointers) and derives the row counts.
+sp_status_t check_desc(const sp_rs_desc_t* d, Problem* pr) {
+  if (!d) return SP_ERR_INVALID_ARG;
+  if (d->dtype != SP_F32 && d->dtype != SP_BF16) return SP_ERR_DTYPE;
+  if (d->norm != SP_RMSNORM && d->norm != SP_LAYERNORM) return SP_ERR_DTYPE;
+  const int nsh = d->nshards == 0 ? 1 : d->nshards;
+  if (d->T < 1 || d->T > kMaxT || d->j < 0 || d->j >= d->T || nsh < 1 || d->j + nsh > d->T ||
+      d->reserved != 0)
+    return SP_ERR_INVALID_ARG;
+  if (!(d->p >= 0.0f && d->p < 1.0f)) return SP_ERR_INVALID_ARG;
+  if (!(d->eps > 0.0f) || !std::isfinite(d->eps)) return SP_ERR_INVALID_ARG;
+  if (d->S < 0 || d->B < 0 || d->H <= 0) return SP_ERR_SHAPE;
+  if (d->S % d->T != 0) return SP_ERR_SHAPE;
+  const int ev = 16 / elem_bytes(d->dtype);
+  if (d->H % ev != 0) return SP_ERR_SHAPE;
+  // row length limit of the register-resident row kernels
+  if (d->H / ev > (int64_t)kMaxFwdTPR * kMaxVPT) return SP_ERR_SHAPE;
+  // every element index must fit comfortably in int64
+  if (d->S > 0 && d->B > 0 && (d->S > ((int64_t)1 << 40) / d->B || d->S * d->B > ((int64_t)1 << 46) / d->H))
+    return SP_ERR_SHAPE;
+  pr->T = d->T;
+  pr->j = d->j;
+  pr->nshards = nsh;
+  pr->dtype = d->dtype;
+  pr->norm = d->norm;
+  pr->S = d->S;
+  pr->B = d->B;
+  pr->H = d->H;
+  pr->R = (d->S / d->T) * d->B;
+  pr->rows = pr->R * nsh;
+  pr->ev = ev;
+  pr->nvec = (int)(d->H / ev);
+  return SP_OK;
+}
+
+// Largest VPT the forward keeps in registers without spilling, by T.
+int fwd_vpt_cap(int T) { return T <= 2 ? 4 : (T <= 4 ? 3 : 2); }
+
+RowShape row_shape(int nvec, int vpt_cap) {
+  int tpr = 32;
+  while (tpr < kMaxFwdTPR && (nvec + tpr - 1) / tpr > vpt_cap) tpr *= 2;
+  RowShape s;
+  s.tpr = tpr;
+  s.vpt = (nvec + tpr - 1) / tpr;
+  s.block = tpr >= 256 ? tpr : 256;
+  return s;
+}
+
+RowShape bwd_row_shape(const Problem& pr) { return row_shape(pr.nvec, pr.ev == 8 ? 2 : 4); }
+
+struct BwdPlan {
+  RowShape shape;
+  size_t smem;
+  int64_t rows_per_cta;
+  int ctas;    // multiple of the cluster size
+  int nparts;  // partial rows per statistic (clusters)
+  size_t ws_bytes;
+};
+
+sp_status_t plan_bwd(const Problem& pr, BwdPlan* pl) {
+  const bool ln = pr.norm == SP_LAYERNORM;
+  pl->shape = bwd_row_shape(pr);
+  pl->smem = (size_t)(ln ? 2 : 1) * (size_t)pr.H * sizeof(float);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SP_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SP_ERR_CUDA;
+  int per_sm = bwd_ctas_per_sm(pr.dtype, ln, pl->shape, pl->smem);
+  if (per_sm < 1) return SP_ERR_CUDA;
+  const int cluster = 8;
+  const int rpc = pl->shape.block / pl->shape.tpr;
+  // as many CTAs as fit at once, but at least one row per row group
+  int64_t want = (pr.rows + rpc - 1) / rpc;
+  int64_t cap = (int64_t)sms * per_sm;
+  int64_t ctas = want < cap ? want : cap;
+  ctas = ((ctas + cluster - 1) / cluster) * cluster;
+  if (ctas < cluster) ctas = cluster;
+  pl->rows_per_cta = pr.rows > 0 ? (pr.rows + ctas - 1) / ctas : 1;
+  pl->ctas = (int)ctas;
+  pl->nparts = (int)(ctas / cluster);
+  pl->ws_bytes = (size_t)pl->nparts * (size_t)pr.H * sizeof(float) * (ln ? 2 : 1);
+  return SP_OK;
+}
+
+sp_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SP_OK : SP_ERR_CUDA; }
+
+}  // namespace
+}  // namespace spf
+
+using namespace spf;
+
+extern "C" {
+
+sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void* const* partials,
+                                            const void* residual, const void* gamma,
+                                            const void* beta, void* h_out, void* y_out,
+                                            uint8_t* mask_out, float* rstd_out, float* mean_out,
+                                            sp_stream_t stream) {
+  Problem pr;
+  sp_status_t st = check_desc(desc, &pr);
+  if (st != SP_OK) return st;
+  const bool ln = pr.norm == SP_LAYERNORM;
+  if (pr.rows == 0) return SP_OK;  // nothing to read or write
+  if (!partials || !residual || !gamma || !h_out || !y_out || !rstd_out) return SP_ERR_INVALID_ARG;
+  if (ln && (!beta || !mean_out)) return SP_ERR_INVALID_ARG;
+  if (desc->p > 0.0f && !mask_out) return SP_ERR_INVALID_ARG;
+  for (int t = 0; t < pr.T; ++t) {
+    if (!partials[t]) return SP_ERR_INVALID_ARG;
+    if (!aligned(partials[t], 16)) return SP_ERR_ALIGN;
+  }
+  if (!aligned(residual, 16) || !aligned(gamma, 16) || !aligned(h_out, 16) || !aligned(y_out, 16) ||
+      (ln && !aligned(beta, 16)) || (mask_out && !aligned(mask_out, 16)) || !aligned(rstd_out, 4) ||
+      (ln && !aligned(mean_out, 4)))
+    return SP_ERR_ALIGN;
+
+  FwdArgs a = {};
+  for (int t = 0; t < pr.T; ++t) a.P[t] = partials[t];
+  a.residual = residual;
+  a.gamma = gamma;
+  a.beta = ln ? beta : nullptr;
+  a.h = h_out;
+  a.y = y_out;
+  a.mask = mask_out;
+  a.rstd = rstd_out;
+  a.mean = ln ? mean_out : nullptr;
+  a.rows = pr.rows;
+  a.grow0 = (int64_t)pr.j * pr.R;
+  a.H = (int32_t)pr.H;
+  a.nvec = pr.nvec;
+  a.thr = (uint32_t)std::floor((double)desc->p * 4294967296.0);
+  a.key0 = (uint32_t)desc->seed;
+  a.key1 = (uint32_t)(desc->seed >> 32);
+  a.scale = (float)(1.0 / (1.0 - (double)desc->p));
+  a.eps = desc->eps;
+  a.Hf = (float)pr.H;
+  a.dropout = desc->p > 0.0f ? 1 : 0;
+
+  const RowShape s = row_shape(pr.nvec, fwd_vpt_cap(pr.T));
+  a.tpr = s.tpr;
+  const int rpc = s.block / s.tpr;
+  const dim3 grid((unsigned)((pr.rows + rpc - 1) / rpc));
+  if (inject_launch_failure()) return SP_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (pr.dtype == SP_BF16)
+    e = ln ? launch_fwd_bf16_ln(a, pr.T, s, grid, cs) : launch_fwd_bf16_rms(a, pr.T, s, grid, cs);
+  else
+    e = ln ? launch_fwd_f32_ln(a, pr.T, s, grid, cs) : launch_fwd_f32_rms(a, pr.T, s, grid, cs);
+  return from_cuda(e);
+}
+
+size_t sp_rs_bwd_workspace_bytes(const sp_rs_desc_t* desc) {
+  Problem pr;
+  if (check_desc(desc, &pr) != SP_OK) return 0;
+  BwdPlan pl;
+  if (plan_bwd(pr, &pl) != SP_OK) return 0;
+  return pl.ws_bytes;
+}
+
+sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc, const void* dy,
+                                            const void* dh_out, const void* h_saved,
+                                            const void* gamma, const uint8_t* mask,
+                                            const float* rstd, const float* mean,
+                                            void* d_residual, void* d_sum, float* dgamma,
+                                            float* dbeta, void* workspace, size_t workspace_bytes,
+                                            sp_stream_t stream) {
+  Problem pr;
+  sp_status_t st = check_desc(desc, &pr);
+  if (st != SP_OK) return st;
+  const bool ln = pr.norm == SP_LAYERNORM;
+  // with no rows only dgamma/dbeta are written (zeros); the rest may be NULL
+  const bool empty = pr.rows == 0;
+  if (!dgamma || (ln && !dbeta)) return SP_ERR_INVALID_ARG;
+  if (!empty && (!dy || !h_saved || !gamma || !rstd || !d_residual || !d_sum))
+    return SP_ERR_INVALID_ARG;
+  if (!empty && ln && !mean) return SP_ERR_INVALID_ARG;
+  if (!empty && desc->p > 0.0f && !mask) return SP_ERR_INVALID_ARG;
+  if (!aligned(dy, 16) || (dh_out && !aligned(dh_out, 16)) || !aligned(h_saved, 16) ||
+      !aligned(gamma, 16) || (mask && !aligned(mask, 16)) || !aligned(rstd, 4) ||
+      (ln && !aligned(mean, 4)) || !aligned(d_residual, 16) || !aligned(d_sum, 16) ||
+      !aligned(dgamma, 16) || (ln && !aligned(dbeta, 16)))
+    return SP_ERR_ALIGN;
+  BwdPlan pl;
+  st = plan_bwd(pr, &pl);
+  if (st != SP_OK) return st;
+  if (!workspace || workspace_bytes < pl.ws_bytes) return SP_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return SP_ERR_ALIGN;
+  if (inject_launch_failure()) return SP_ERR_CUDA;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  float* ws = static_cast<float*>(workspace);
+  int nparts = 0;
+  if (pr.rows > 0) {
+    BwdArgs a = {};
+    a.dy = dy;
+    a.dh = dh_out;
+    a.h = h_saved;
+    a.gamma = gamma;
+    a.mask = desc->p > 0.0f ? mask : nullptr;
+    a.rstd = rstd;
+    a.mean = ln ? mean : nullptr;
+    a.d_res = d_residual;
+    a.d_sum = d_sum;
+    a.ws = ws;
+    a.rows = pr.rows;
+    a.rows_per_cta = pl.rows_per_cta;
+    a.H = (int32_t)pr.H;
+    a.nvec = pr.nvec;
+    a.tpr = pl.shape.tpr;
+    a.nparts = pl.nparts;
+    a.scale = (float)(1.0 / (1.0 - (double)desc->p));
+    a.Hf = (float)pr.H;
+    cudaError_t e = launch_bwd(pr.dtype, ln, a, pl.shape, dim3((unsigned)pl.ctas), pl.smem, cs);
+    if (e != cudaSuccess) return SP_ERR_CUDA;
+    nparts = pl.nparts;
+  }
+  return from_cuda(launch_colsum(ws, nparts, (int)pr.H, ln, dgamma, ln ? dbeta : nullptr, cs));
+}
+
+static sp_status_t layout_call(bool to_hp, const void* in, void* out, int64_t N, int64_t H,
+                               int32_t T, int32_t dtype, sp_stream_t stream) {
+  if (dtype != SP_F32 && dtype != SP_BF16) return SP_ERR_DTYPE;
+  if (!in || !out) return SP_ERR_INVALID_ARG;
+  if (T < 1 || T > kMaxT) return SP_ERR_INVALID_ARG;
+  if (N < 0 || H <= 0 || N % T != 0 || H % T != 0) return SP_ERR_SHAPE;
+  const int ev = 16 / elem_bytes(dtype);
+  if ((H / T) % ev != 0) return SP_ERR_SHAPE;
+  if (N > 0 && N > ((int64_t)1 << 50) / H) return SP_ERR_SHAPE;
+  if (!aligned(in, 16) || !aligned(out, 16)) return SP_ERR_ALIGN;
+  if (inject_launch_failure()) return SP_ERR_CUDA;
+  return from_cuda(launch_layout(to_hp, in, out, N, H, T, elem_bytes(dtype),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sp_status_t sp2hp(const void* in, void* out, int64_t N, int64_t H, int32_t T, int32_t dtype,
+                  sp_stream_t stream) {
+  return layout_call(true, in, out, N, H, T, dtype, stream);
+}
+
+sp_status_t hp2sp(const void* in, void* out, int64_t N, int64_t H, int32_t T, int32_t dtype,
+                  sp_stream_t stream) {
+  return layout_call(false, in, out, N, H, T, dtype, stream);
+}
+
+const char* sp_status_string(sp_status_t s) {
+  switch (s) {
+    case SP_OK: return "SP_OK";
+    case SP_ERR_INVALID_ARG: return "SP_ERR_INVALID_ARG: invalid argument";
+    case SP_ERR_SHAPE: return "SP_ERR_SHAPE: unsupported or inconsistent shape";
+    case SP_ERR_ALIGN: return "SP_ERR_ALIGN: pointer not aligned as required";
+    case SP_ERR_DTYPE: return "SP_ERR_DTYPE: unknown dtype or norm";
+    case SP_ERR_WORKSPACE: return "SP_ERR_WORKSPACE: workspace missing or too small";
+    case SP_ERR_CUDA: return "SP_ERR_CUDA: CUDA runtime error";
+    case SP_ERR_NOT_IMPLEMENTED: return "SP_ERR_NOT_IMPLEMENTED";
+    default: return "unknown sp_status_t";
+  }
+}
+
+int32_t sp_version(void) { return 100; }
+
+}  // extern "C"

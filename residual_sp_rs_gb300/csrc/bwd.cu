@@ -1,0 +1,56 @@
+// bwd.cu -- backward instances (activation x norm x VPT) and launchers.
+#include "bwd.cuh"
+#include "launch.h"
+
+namespace spf {
+
+namespace {
+
+template <typename Act, bool LN>
+void (*bwd_kernel_for(int vpt))(const BwdArgs) {
+  switch (vpt) {
+    case 1: return sp_bwd_kernel<Act, LN, 1>;
+    case 2: return sp_bwd_kernel<Act, LN, 2>;
+    case 3: return sp_bwd_kernel<Act, LN, 3>;
+    case 4: return sp_bwd_kernel<Act, LN, 4>;
+    default: return nullptr;
+  }
+}
+
+void (*bwd_kernel(int dtype, bool ln, int vpt))(const BwdArgs) {
+  if (dtype == 1) return ln ? bwd_kernel_for<__nv_bfloat16, true>(vpt) : bwd_kernel_for<__nv_bfloat16, false>(vpt);
+  return ln ? bwd_kernel_for<float, true>(vpt) : bwd_kernel_for<float, false>(vpt);
+}
+
+}  // namespace
+
+int bwd_ctas_per_sm(int dtype, bool ln, const RowShape& s, size_t smem) {
+  void (*k)(const BwdArgs) = bwd_kernel(dtype, ln, s.vpt);
+  if (!k) return 0;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, s.block, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_bwd(int dtype, bool ln, const BwdArgs& a, const RowShape& s, dim3 grid,
+                       size_t smem, cudaStream_t st) {
+  void (*k)(const BwdArgs) = bwd_kernel(dtype, ln, s.vpt);
+  if (!k) return cudaErrorInvalidValue;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return pdl_launch(k, grid, dim3(s.block), smem, st, a);
+}
+
+cudaError_t launch_colsum(const float* ws, int nparts, int H, bool ln, float* dgamma,
+                          float* dbeta, cudaStream_t st) {
+  const int n4 = H / 4;
+  const dim3 grid((unsigned)((n4 + 31) / 32), ln ? 2u : 1u);
+  return pdl_launch(sp_colsum_kernel, grid, dim3(32, 8), 0, st, ws, nparts, H, dgamma, dbeta);
+}
+
+}  // namespace spf

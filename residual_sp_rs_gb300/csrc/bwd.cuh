@@ -1,0 +1,225 @@
+// bwd.cuh -- backward of the SP region (norm backward, residual-add and
+// dropout backward) and the first pass of the dgamma/dbeta reduction.
+//
+// A persistent-style grid: CTA b owns the contiguous rows
+// [b*rows_per_cta, (b+1)*rows_per_cta); its row groups walk those rows one
+// row at a time.  A thread owns the same columns on every row, so its
+// dgamma/dbeta contributions accumulate in registers across rows.  At the end
+// the CTA adds its row groups' sums in row-group order into shared memory;
+// the 8 CTAs of a thread-block cluster then add their sums through
+// distributed shared memory in rank order and write one fp32 partial row per
+// statistic per cluster; sp_colsum_kernel adds the partial rows in cluster
+// order.  The result is bit-identical from run to run.
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace spf {
+
+namespace cg = cooperative_groups;
+
+constexpr int kBwdCluster = 8;  // CTAs per thread-block cluster in the backward
+
+template <typename Act, bool LN, int VPT>
+__global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
+    sp_bwd_kernel(const BwdArgs a) {
+  using V = Act16<Act>;
+  constexpr int EV = V::EV;
+  constexpr int NS = LN ? 2 : 1;  // row sums needed: mean(g*xhat) (+ mean(g))
+  __shared__ float red[2 * 32 * 2];
+  extern __shared__ float colacc[];  // [NS][H] CTA column sums
+
+  const int tpr = a.tpr;
+  const int rg = threadIdx.x / tpr;
+  const int lr = threadIdx.x - rg * tpr;
+  const int rpc = blockDim.x / tpr;
+  const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_cta;
+  const int64_t r1 = min(a.rows, r0 + a.rows_per_cta);
+
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+
+  float gm[VPT][EV];
+  float dg[VPT][EV];
+  float db[LN ? VPT : 1][EV];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lr + k * tpr;
+#pragma unroll
+    for (int e = 0; e < EV; ++e) {
+      gm[k][e] = 0.f;
+      dg[k][e] = 0.f;
+      if constexpr (LN) db[k][e] = 0.f;
+    }
+    if (v < a.nvec) V::unpack(ld_cached(reinterpret_cast<const Act*>(a.gamma) + v * EV), gm[k]);
+  }
+
+  float* rred = red + rg * 2 * (tpr >> 5) * NS;
+  int slot = 0;
+  for (int64_t r = r0 + rg; r < r1; r += rpc) {
+    const int64_t ro = r * (int64_t)a.H;
+    uint4 dyv[VPT], dhv[VPT], hv[VPT];
+    uint32_t mk[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lr + k * tpr;
+      if (v < a.nvec) {
+        const int64_t o = ro + (int64_t)v * EV;
+        dyv[k] = ld_stream(reinterpret_cast<const Act*>(a.dy) + o);
+        hv[k] = ld_stream(reinterpret_cast<const Act*>(a.h) + o);
+        if (a.dh) dhv[k] = ld_stream(reinterpret_cast<const Act*>(a.dh) + o);
+        mk[k] = a.mask ? ld_mask<EV>(a.mask + o) : (1u << EV) - 1u;
+      }
+    }
+    const float rstd = __ldcs(a.rstd + r);
+    const float mu = LN ? __ldcs(a.mean + r) : 0.f;
+
+    float xh[VPT][EV], dyf[VPT][EV];
+    float sums[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) sums[i] = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lr + k * tpr;
+#pragma unroll
+      for (int e = 0; e < EV; ++e) {
+        xh[k][e] = 0.f;
+        dyf[k][e] = 0.f;
+      }
+      if (v < a.nvec) {
+        float hf[EV];
+        V::unpack(dyv[k], dyf[k]);
+        V::unpack(hv[k], hf);
+#pragma unroll
+        for (int e = 0; e < EV; ++e) {
+          xh[k][e] = (hf[e] - mu) * rstd;
+          const float g = gm[k][e] * dyf[k][e];
+          sums[0] += g * xh[k][e];
+          if constexpr (LN) sums[1] += g;
+        }
+      }
+    }
+    row_allreduce<NS>(sums, tpr, lr, 1 + rg, rred, slot);
+    slot ^= 1;
+    const float c_gx = sums[0] / a.Hf;
+    const float c_g = LN ? sums[NS - 1] / a.Hf : 0.f;
+
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lr + k * tpr;
+      if (v < a.nvec) {
+        float dhf[EV], dres[EV], dsum[EV];
+        if (a.dh) {
+          V::unpack(dhv[k], dhf);
+        } else {
+#pragma unroll
+          for (int e = 0; e < EV; ++e) dhf[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < EV; ++e) {
+          const float g = gm[k][e] * dyf[k][e];
+          const float dHn = rstd * (g - c_g - xh[k][e] * c_gx);
+          dres[e] = dHn + dhf[e];
+          dsum[e] = ((mk[k] >> e) & 1u) ? dres[e] * a.scale : 0.f;
+          dg[k][e] += dyf[k][e] * xh[k][e];
+          if constexpr (LN) db[k][e] += dyf[k][e];
+        }
+        const int64_t o = ro + (int64_t)v * EV;
+        st_stream(reinterpret_cast<Act*>(a.d_res) + o, V::pack(dres));
+        st_stream(reinterpret_cast<Act*>(a.d_sum) + o, V::pack(dsum));
+      }
+    }
+  }
+
+  // ---- CTA column sums in row-group order ---------------------------------
+  for (int q = 0; q < rpc; ++q) {
+    if (rg == q) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = lr + k * tpr;
+        if (v < a.nvec) {
+#pragma unroll
+          for (int e = 0; e < EV; ++e) {
+            const int c = v * EV + e;
+            colacc[c] = (q == 0) ? dg[k][e] : colacc[c] + dg[k][e];
+            if constexpr (LN) colacc[a.H + c] = (q == 0) ? db[k][e] : colacc[a.H + c] + db[k][e];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- cluster column sums over distributed shared memory -----------------
+  // CTA rank q of the cluster adds column slice q of all kBwdCluster CTAs'
+  // sums, in rank order, and writes it to the cluster's partial row; the
+  // second pass then reads one row per cluster instead of one per CTA.
+  cg::cluster_group cl = cg::this_cluster();
+  cl.sync();
+  const int q = (int)cl.block_rank();
+  const int n4 = a.H >> 2;
+  const int per = (n4 + kBwdCluster - 1) / kBwdCluster;
+  const int c_end = min(n4, (q + 1) * per);
+  const int64_t cluster_id = blockIdx.x / kBwdCluster;
+#pragma unroll
+  for (int st = 0; st < NS; ++st) {
+    float4* out = reinterpret_cast<float4*>(a.ws + ((int64_t)st * a.nparts + cluster_id) * a.H);
+    for (int c4 = q * per + (int)threadIdx.x; c4 < c_end; c4 += blockDim.x) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int p = 0; p < kBwdCluster; ++p) {
+        const float4 w =
+            reinterpret_cast<const float4*>(cl.map_shared_rank(colacc + st * a.H, p))[c4];
+        s.x += w.x;
+        s.y += w.y;
+        s.z += w.z;
+        s.w += w.w;
+      }
+      __stcg(out + c4, s);
+    }
+  }
+  cl.sync();  // keep this CTA's shared memory alive until every peer has read it
+}
+
+// Second pass: dgamma[c] (and dbeta[c]) = sum over partial rows p = 0..nparts-1
+// in that order.  blockDim (32, 8): x picks a float4 column group, y a stride
+// class of partial rows; the 8 stride sums are added in y order.
+__global__ void __launch_bounds__(256) sp_colsum_kernel(const float* ws, int nparts, int H,
+                                                        float* dgamma, float* dbeta) {
+  __shared__ float4 part[8][32];
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  const int stat = blockIdx.y;
+  const float* src = ws + (int64_t)stat * nparts * H;
+  float* dst = stat ? dbeta : dgamma;
+  const int c4 = blockIdx.x * 32 + threadIdx.x;
+  const int n4 = H / 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c4 < n4) {
+    for (int p = threadIdx.y; p < nparts; p += 8) {
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)p * H) + c4);
+      acc.x += w.x;
+      acc.y += w.y;
+      acc.z += w.z;
+      acc.w += w.w;
+    }
+  }
+  part[threadIdx.y][threadIdx.x] = acc;
+  __syncthreads();
+  if (threadIdx.y == 0 && c4 < n4) {
+    float4 s = part[0][threadIdx.x];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) {
+      const float4 w = part[q][threadIdx.x];
+      s.x += w.x;
+      s.y += w.y;
+      s.z += w.z;
+      s.w += w.w;
+    }
+    reinterpret_cast<float4*>(dst)[c4] = s;
+  }
+}
+
+}  // namespace spf

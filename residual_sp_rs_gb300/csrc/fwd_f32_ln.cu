@@ -1,0 +1,9 @@
+// Forward instances: activation f32, norm ln.
+#include "fwd_inst.cuh"
+
+namespace spf {
+cudaError_t launch_fwd_f32_ln(const FwdArgs& a, int T, const RowShape& s, dim3 grid,
+                                  cudaStream_t st) {
+  return launch_fwd_impl<float, true>(a, T, s, grid, st);
+}
+}  // namespace spf

@@ -1,0 +1,55 @@
+// launch.h -- host-side launch helpers and the internal launcher table of
+// libspfuse (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace spf {
+
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while the previous kernel in the stream drains; it does not read
+// memory before griddepcontrol.wait, so stream order is kept.
+template <typename... KArgs, typename... Args>
+inline cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Row kernel shape: threads per row, 16-byte vectors per thread, block size.
+struct RowShape {
+  int tpr;
+  int vpt;
+  int block;
+};
+
+// Forward launchers, one translation unit per (activation, norm); T in 1..8
+// and VPT in 1..4 are compile-time.
+cudaError_t launch_fwd_bf16_rms(const FwdArgs& a, int T, const RowShape& s, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_bf16_ln(const FwdArgs& a, int T, const RowShape& s, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_f32_rms(const FwdArgs& a, int T, const RowShape& s, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_f32_ln(const FwdArgs& a, int T, const RowShape& s, dim3 grid, cudaStream_t st);
+
+// Backward launchers (VPT in 1..4) and their occupancy (CTAs per SM).
+cudaError_t launch_bwd(int dtype, bool ln, const BwdArgs& a, const RowShape& s, dim3 grid,
+                       size_t smem, cudaStream_t st);
+int bwd_ctas_per_sm(int dtype, bool ln, const RowShape& s, size_t smem);
+cudaError_t launch_colsum(const float* ws, int nparts, int H, bool ln, float* dgamma,
+                          float* dbeta, cudaStream_t st);
+
+cudaError_t launch_layout(bool to_hp, const void* in, void* out, int64_t N, int64_t H, int32_t T,
+                          int elem_bytes, cudaStream_t stream);
+
+}  // namespace spf

@@ -1,0 +1,172 @@
+"""Host-side tests of libspfuse that need no GPU: the library builds for
+sm_103a, loads, exports every entry point include/spfuse.h declares, and
+rejects invalid arguments before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+import textwrap
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spfuse.h")
+
+
+@pytest.fixture(scope="module")
+def spf():
+    from residual_sp_rs_gb300 import build, ops
+    build.build()
+    return ops
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(sp\w*|hp2sp)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["sp_rs_dropout_residual_norm_fwd", "sp_rs_bwd_workspace_bytes",
+              "sp_rs_dropout_residual_norm_bwd", "sp2hp", "hp2sp", "sp_status_string", "sp_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(spf):
+    lib = spf.lib()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", spf.LIB_PATH], capture_output=True, text=True)
+    if out.returncode == 0:
+        exported = {l.split()[-1] for l in out.stdout.splitlines() if l.strip()}
+        for n in declared_functions():
+            assert n in exported, n
+
+
+def test_library_is_built_for_sm_103a(spf):
+    out = subprocess.run(["cuobjdump", "--list-elf", spf.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_struct_layout_matches_header(spf):
+    assert ctypes.sizeof(spf.SpRsDesc) == 64
+    assert spf.SpRsDesc.seed.offset == 48 and spf.SpRsDesc.nshards.offset == 56
+
+
+def test_status_strings(spf):
+    for code in range(8):
+        assert spf.status_string(code).startswith("SP_")
+    assert spf.lib().sp_version() >= 100
+
+
+FAKE = 1 << 20   # a 16-byte aligned address that is never dereferenced
+
+
+def _fwd(spf, desc, partials=None, residual=FAKE, gamma=FAKE, beta=FAKE, h=FAKE, y=FAKE, mask=FAKE,
+         rstd=FAKE, mean=FAKE):
+    partials = [FAKE] * desc.T if partials is None else partials
+    arr = (ctypes.c_void_p * max(1, len(partials)))(*partials)
+    return spf.lib().sp_rs_dropout_residual_norm_fwd(ctypes.byref(desc), arr, residual, gamma, beta,
+                                                    h, y, mask, rstd, mean, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), 1), (dict(T=9), 1), (dict(j=2), 1), (dict(j=-1), 1), (dict(nshards=3), 1),
+    (dict(p=1.0), 1), (dict(p=-0.1), 1), (dict(p=float("nan")), 1), (dict(eps=0.0), 1),
+    (dict(eps=float("inf")), 1), (dict(S=15), 2), (dict(H=12), 2), (dict(H=16392), 2),
+    (dict(S=-2), 2), (dict(dtype=7), 4), (dict(norm=3), 4),
+])
+def test_fwd_rejects_bad_descriptors(spf, kw, code):
+    base = dict(T=2, j=0, S=16, B=2, H=64, dtype="bf16", norm="rms", p=0.1, eps=1e-6, seed=0)
+    base.update(kw)
+    desc = spf.make_desc(**base)
+    assert _fwd(spf, desc) == code
+
+
+def test_fwd_rejects_bad_pointers(spf):
+    d = spf.make_desc(2, 0, 16, 2, 64, "bf16", "ln", 0.1, 1e-5)
+    assert _fwd(spf, d, partials=[FAKE, 0]) == 1
+    assert _fwd(spf, d, residual=0) == 1
+    assert _fwd(spf, d, beta=0) == 1            # LayerNorm needs beta
+    assert _fwd(spf, d, mean=0) == 1            # ... and mean
+    assert _fwd(spf, d, mask=0) == 1            # p > 0 needs the mask
+    assert _fwd(spf, d, partials=[FAKE, FAKE + 8]) == 3
+    assert _fwd(spf, d, y=FAKE + 2) == 3
+    assert _fwd(spf, d, rstd=FAKE + 2) == 3
+    d0 = spf.make_desc(2, 0, 16, 2, 64, "bf16", "rms", 0.0, 1e-5)
+    d0.reserved = 1
+    assert _fwd(spf, d0) == 1
+
+
+def test_empty_problem_launches_nothing(spf):
+    d = spf.make_desc(2, 0, 0, 2, 64, "bf16", "rms", 0.1, 1e-6)
+    assert _fwd(spf, d) == 0   # S = 0: nothing to do, no device touched
+
+
+def test_bwd_rejects_bad_arguments(spf):
+    L = spf.lib()
+    d = spf.make_desc(2, 0, 16, 2, 64, "bf16", "rms", 0.1, 1e-6)
+
+    def call(desc, mask=FAKE, dy=FAKE, ws=FAKE, nbytes=1 << 30):
+        return L.sp_rs_dropout_residual_norm_bwd(ctypes.byref(desc), dy, FAKE, FAKE, FAKE, mask, FAKE,
+                                                 FAKE, FAKE, FAKE, FAKE, FAKE, ws, nbytes, None)
+    assert call(d, mask=0) == 1
+    assert call(d, dy=0) == 1
+    assert call(d, dy=FAKE + 4) == 3
+    bad = spf.make_desc(3, 0, 16, 2, 64, "bf16", "rms", 0.1, 1e-6)
+    assert call(bad) == 2
+    assert L.sp_rs_bwd_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, FAKE, 16, 64, 4, 9), 4), ((0, FAKE, 16, 64, 4, 1), 1), ((FAKE, FAKE, 15, 64, 4, 1), 2),
+    ((FAKE, FAKE, 16, 48, 4, 1), 2), ((FAKE, FAKE, 16, 64, 9, 1), 1), ((FAKE + 4, FAKE, 16, 64, 4, 1), 3),
+])
+def test_layout_rejects_bad_arguments(spf, args, code):
+    L = spf.lib()
+    assert L.sp2hp(*args, None) == code
+    assert L.hp2sp(*args, None) == code
+
+
+def test_launch_failure_is_reported(spf):
+    """A failing launch (injected on the host) comes back as SP_ERR_CUDA."""
+    code = textwrap.dedent(f"""
+        import ctypes, sys
+        sys.path.insert(0, {ROOT!r})
+        from residual_sp_rs_gb300 import ops
+        d = ops.make_desc(2, 0, 16, 2, 64, "bf16", "rms", 0.1, 1e-6)
+        arr = (ctypes.c_void_p * 2)({FAKE}, {FAKE})
+        L = ops.lib()
+        r1 = L.sp_rs_dropout_residual_norm_fwd(ctypes.byref(d), arr, {FAKE}, {FAKE}, None, {FAKE},
+                                               {FAKE}, {FAKE}, {FAKE}, None, None)
+        r2 = L.sp2hp({FAKE}, {FAKE}, 16, 64, 4, 1, None)
+        print(r1, r2)
+    """)
+    env = dict(os.environ, SPFUSE_FAIL_LAUNCH="1")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["6", "6"]
+
+
+def test_python_binding_raises_on_error(spf):
+    d = spf.make_desc(2, 0, 15, 2, 64, "bf16", "rms", 0.1, 1e-6)
+    with pytest.raises(RuntimeError, match="SP_ERR_SHAPE"):
+        spf.sp_rs_dropout_residual_norm_fwd(d, [FAKE, FAKE], FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE,
+                                            None, stream=0)
+
+
+def test_product_package_does_not_import_oracle():
+    """The product path never reaches the oracle."""
+    pkg = os.path.join(ROOT, "residual_sp_rs_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt, f
+                assert "oracle.h" not in txt and "liboracle" not in txt, f

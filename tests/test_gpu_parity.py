@@ -1,0 +1,411 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Inputs come from residual_sp_rs_gb300.synthetic (seeded, shared by both
+sides); expected values come only from the oracle.  Small and mid-size
+workloads are compared element by element; the large-hidden workload is
+compared on sampled rows (all outputs), with the dropout mask checked over
+every element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from residual_sp_rs_gb300 import ops, synthetic as syn
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from residual_sp_rs_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _np(t):
+    return syn.to_storage(t)
+
+
+def _desc(w, j, nshards=1, p=None, seed=None):
+    return ops.make_desc(w.T, j, w.S, w.B, w.H, w.dtype, w.norm, w.p if p is None else p, w.eps,
+                         w.seed if seed is None else seed, nshards)
+
+
+def _oracle_problem(w, j, nshards=1, p=None, seed=None):
+    pf = float(np.float32(w.p if p is None else p))
+    return oracle.problem(w.T, j, w.S, w.B, w.H, w.dtype, w.norm, pf, float(np.float32(w.eps)),
+                          w.seed if seed is None else seed, nshards)
+
+
+def _gpu_fwd(w, inp, j, nshards=1, p=None, seed=None, with_mask=True):
+    d = _desc(w, j, nshards, p, seed)
+    R = w.R
+    res = inp["residual"].view(w.S * w.B, w.H)[j * R:(j + nshards) * R]
+    out = ops.forward(d, inp["partials"], res, inp["gamma"], inp["beta"])
+    if not with_mask and d.p == 0:
+        assert out["mask"] is None
+    return out
+
+
+def _host(out):
+    return {k: (None if v is None else _np(v)) for k, v in out.items()}
+
+
+def _full_fwd_check(w, inp, j, nshards=1, p=None, seed=None):
+    out = _gpu_fwd(w, inp, j, nshards, p, seed)
+    torch.cuda.synchronize()
+    pr = _oracle_problem(w, j, nshards, p, seed)
+    R = w.R
+    res = _np(inp["residual"]).reshape(w.S * w.B, w.H)[j * R:(j + nshards) * R]
+    parts = [_np(t) for t in inp["partials"]]
+    orc = oracle.fwd(pr, parts, res, _np(inp["gamma"]),
+                     None if inp["beta"] is None else _np(inp["beta"]), w.dtype)
+    g = _host(out)
+    if g["mask"] is None:
+        g["mask"] = np.ones_like(orc["mask"])
+    if g["mean"] is None:
+        g["mean"] = np.zeros(len(orc["rstd"]))
+    parity.compare_fwd(w.dtype, w.norm, g, orc, oracle.to_f64(_np(inp["gamma"]), w.dtype))
+    return out, orc
+
+
+# ---------------------------------------------------------------------------
+# forward
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("j", [0, 1])
+def test_fwd_tiny_rms_f32(j):
+    w = syn.WORKLOADS["tiny_rms_f32"]
+    inp = syn.fwd_inputs(w, DEV)
+    _full_fwd_check(w, inp, j)
+
+
+def test_fwd_pages_shape_bf16_all_shards_and_single():
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    both, _ = _full_fwd_check(w, inp, 0, nshards=2)
+    for j in range(2):
+        one, _ = _full_fwd_check(w, inp, j)
+        R = w.R
+        for k in ["h", "y", "mask", "rstd"]:   # one launch over both shards == two launches
+            assert torch.equal(one[k], both[k][j * R:(j + 1) * R] if k != "rstd"
+                               else both[k][j * R:(j + 1) * R])
+
+
+def test_fwd_gpt_layernorm_every_shard():
+    w = syn.WORKLOADS["gpt_ln_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    for j in range(w.T):
+        _full_fwd_check(w, inp, j)
+
+
+def _sample_rows(R, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = set([0, 1, R - 2, R - 1]) | set(int(x) for x in rng.integers(0, R, n))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("p", [0.1, 0.0])
+def test_fwd_large_hidden_every_shard_sampled(p):
+    w = syn.WORKLOADS["large_rms_bf16"].with_(p=p)
+    inp = syn.fwd_inputs(w, DEV)
+    R, H = w.R, w.H
+    gam = _np(inp["gamma"])
+    flat_parts = [t.view(w.S * w.B, H) for t in inp["partials"]]
+    flat_res = inp["residual"].view(w.S * w.B, H)
+    for j in range(w.T):
+        out = _gpu_fwd(w, inp, j)
+        torch.cuda.synchronize()
+        if p > 0:   # the whole mask, bit-exact
+            ref = oracle.mask_range(w.seed, float(np.float32(p)), j * R * H, R * H)
+            assert np.array_equal(_np(out["mask"]).ravel(), ref), f"mask shard {j}"
+        rows = _sample_rows(R, 40, 100 + j)
+        grows = j * R + rows
+        idx = torch.from_numpy(grows).to(DEV)
+        prows = [_np(fp.index_select(0, idx)) for fp in flat_parts]
+        orc = oracle.fwd_rows(_oracle_problem(w, j), grows, prows, _np(flat_res.index_select(0, idx)),
+                              gam, None, w.dtype)
+        ridx = torch.from_numpy(rows).to(DEV)
+        g = dict(h=_np(out["h"].index_select(0, ridx)), y=_np(out["y"].index_select(0, ridx)),
+                 mask=(_np(out["mask"].index_select(0, ridx)) if out["mask"] is not None
+                       else np.ones((len(rows), H), np.uint8)),
+                 rstd=_np(out["rstd"][ridx]), mean=np.zeros(len(rows)))
+        parity.compare_fwd(w.dtype, w.norm, g, orc, oracle.to_f64(gam, w.dtype))
+        del out
+
+
+@pytest.mark.parametrize("case", [
+    # (T, S, B, H, dtype, norm, p): ragged tails, minimum/maximum widths, T = 1, odd T
+    (3, 21, 1, 776, "bf16", "rms", 0.1),
+    (3, 21, 1, 776, "bf16", "ln", 0.3),
+    (1, 5, 3, 8, "bf16", "rms", 0.5),
+    (8, 16, 3, 64, "bf16", "ln", 0.1),
+    (2, 6, 1, 16384, "bf16", "rms", 0.1),
+    (5, 10, 2, 4104, "bf16", "ln", 0.2),
+    (2, 4, 5, 8192, "f32", "ln", 0.1),
+    (4, 8, 3, 12, "f32", "rms", 0.7),
+    (7, 14, 1, 1032, "f32", "ln", 0.0),
+])
+def test_fwd_edge_shapes(case):
+    T, S, B, H, dt, nm, p = case
+    w = syn.Workload("edge", T, S, B, H, dt, nm, p, 1e-5, 0x0123456789ABCDEF, 0.5, 1.0, 0.5, 1.5, 0.1,
+                     4242 + H)
+    inp = syn.fwd_inputs(w, DEV)
+    for j in sorted({0, T - 1}):
+        _full_fwd_check(w, inp, j)
+    _full_fwd_check(w, inp, 0, nshards=T)
+
+
+def test_fwd_p0_without_mask_is_exact_residual_add():
+    w = syn.WORKLOADS["pages_rms_bf16"].with_(p=0.0)
+    inp = syn.fwd_inputs(w, DEV)
+    d = _desc(w, 1)
+    R = w.R
+    res = inp["residual"].view(-1, w.H)[R:2 * R]
+    out = ops.forward(d, inp["partials"], res, inp["gamma"])
+    assert out["mask"] is None
+    torch.cuda.synchronize()
+    pr = _oracle_problem(w, 1)
+    orc = oracle.fwd(pr, [_np(t) for t in inp["partials"]], _np(res), _np(inp["gamma"]), None, "bf16")
+    g = _host(out)
+    g["mask"] = np.ones_like(orc["mask"])
+    g["mean"] = np.zeros(R)
+    parity.compare_fwd("bf16", "rms", g, orc, oracle.to_f64(_np(inp["gamma"]), "bf16"))
+
+
+def test_fwd_empty_rows_is_a_no_op():
+    w = syn.WORKLOADS["pages_rms_bf16"].with_(S=0)
+    d = _desc(w, 0)
+    z = torch.empty((0, w.H), device=DEV, dtype=torch.bfloat16)
+    g = torch.ones(w.H, device=DEV, dtype=torch.bfloat16)
+    ops.sp_rs_dropout_residual_norm_fwd(d, [z, z], z, g, None, z, z,
+                                        torch.empty((0, w.H), device=DEV, dtype=torch.uint8),
+                                        torch.empty(0, device=DEV), None)
+    torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# backward
+# ---------------------------------------------------------------------------
+
+def _bwd_inputs_from_oracle_fwd(w, j, nshards, inp, grads):
+    """Saved activations for the backward = the ORACLE forward's outputs."""
+    pr = _oracle_problem(w, j, nshards)
+    R = w.R
+    res = _np(inp["residual"]).reshape(-1, w.H)[j * R:(j + nshards) * R]
+    orc = oracle.fwd(pr, [_np(t) for t in inp["partials"]], res, _np(inp["gamma"]),
+                     None if inp["beta"] is None else _np(inp["beta"]), w.dtype)
+    tdt = syn.torch_dtype(w.dtype)
+    dev = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to(DEV) if dt is None else \
+        syn.from_storage(a, dt).to(DEV)
+    saved = dict(h=dev(orc["h"], w.dtype), mask=dev(orc["mask"]),
+                 rstd=dev(orc["rstd"].astype(np.float32)), mean=dev(orc["mean"].astype(np.float32)))
+    dy = grads["dy"].view(-1, w.H)[j * R:(j + nshards) * R]
+    dh = grads["dh_out"].view(-1, w.H)[j * R:(j + nshards) * R]
+    return pr, orc, saved, dy, dh
+
+
+def _check_bwd(w, pr, saved_np, dy_np, dh_np, gamma_np, mask_np, gout):
+    orc = oracle.bwd(pr, dy_np, dh_np, saved_np, gamma_np, mask_np, w.dtype)
+    g = _host(gout)
+    parity.check_act("d_residual", w.dtype, g["d_res"], orc["dres_exact"])
+    parity.check_act("d_sum", w.dtype, g["d_sum"], orc["dsum_exact"])
+    parity.check_reduction("dgamma", g["dgamma"], orc["dgamma"])
+    if w.norm == "ln":
+        parity.check_reduction("dbeta", g["dbeta"], orc["dbeta"])
+
+
+@pytest.mark.parametrize("name,j,nshards", [("tiny_rms_f32", 0, 1), ("tiny_rms_f32", 1, 1),
+                                            ("pages_rms_bf16", 0, 1), ("pages_rms_bf16", 0, 2),
+                                            ("gpt_ln_bf16", 3, 1), ("gpt_ln_bf16", 0, 8)])
+@pytest.mark.parametrize("with_dh", [True, False])
+def test_bwd_parity(name, j, nshards, with_dh):
+    w = syn.WORKLOADS[name]
+    inp = syn.fwd_inputs(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    pr, orc_f, saved, dy, dh = _bwd_inputs_from_oracle_fwd(w, j, nshards, inp, grads)
+    d = _desc(w, j, nshards)
+    out = ops.backward(d, dy, dh if with_dh else None, saved["h"], inp["gamma"], saved["mask"],
+                       saved["rstd"], saved["mean"] if w.norm == "ln" else None)
+    torch.cuda.synchronize()
+    _check_bwd(w, pr, orc_f["h"], _np(dy), _np(dh) if with_dh else None, _np(inp["gamma"]),
+               orc_f["mask"], out)
+
+
+@pytest.mark.parametrize("p", [0.1, 0.0])
+def test_bwd_large_hidden_sampled(p):
+    w = syn.WORKLOADS["large_rms_bf16"].with_(p=p)
+    saved = syn.saved_activations(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    gam = syn.fwd_inputs(w.with_(T=1, S=1, B=1), DEV)["gamma"]   # gamma only
+    R, H = w.R, w.H
+    for j in [0, 5, 7]:
+        sl = slice(j * R, (j + 1) * R)
+        h = saved["h"].view(-1, H)[sl]
+        pr = _oracle_problem(w, j, p=p)
+        h_np = _np(h)
+        rstd, mean = oracle.norm_stats(pr, h_np, w.dtype)     # row statistics from the oracle
+        rstd_t = torch.from_numpy(rstd.astype(np.float32)).to(DEV)
+        dy = grads["dy"].view(-1, H)[sl]
+        dh = grads["dh_out"].view(-1, H)[sl]
+        mask = saved["mask"].view(-1, H)[sl] if p > 0 else None
+        d = _desc(w, j, p=p)
+        out = ops.backward(d, dy, dh, h, gam, mask, rstd_t)
+        torch.cuda.synchronize()
+        # dgamma needs every row: full oracle backward for this shard
+        full = oracle.bwd(pr, _np(dy), _np(dh), h_np, _np(gam), None if mask is None else _np(mask))
+        parity.check_reduction("dgamma", _np(out["dgamma"]), full["dgamma"])
+        rows = _sample_rows(R, 40, 300 + j)
+        ridx = torch.from_numpy(rows).to(DEV)
+        for key, ex in [("d_res", "dres_exact"), ("d_sum", "dsum_exact")]:
+            parity.check_bf16(key, _np(out[key].index_select(0, ridx)), full[ex][rows])
+        del out, full
+
+
+@pytest.mark.parametrize("case", [
+    (3, 21, 1, 776, "bf16", "ln", 0.3), (1, 5, 3, 8, "bf16", "rms", 0.5),
+    (2, 6, 1, 16384, "bf16", "ln", 0.1), (5, 10, 2, 4104, "bf16", "rms", 0.2),
+    (2, 4, 5, 8192, "f32", "ln", 0.1), (4, 8, 3, 12, "f32", "rms", 0.7), (7, 14, 1, 1032, "f32", "ln", 0.0),
+    (2, 2000, 1, 768, "bf16", "rms", 0.1),
+])
+def test_bwd_edge_shapes(case):
+    T, S, B, H, dt, nm, p = case
+    w = syn.Workload("edge", T, S, B, H, dt, nm, p, 1e-5, 7, 0.5, 1.0, 0.5, 1.5, 0.1, 999 + H)
+    inp = syn.fwd_inputs(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    for j, nsh in sorted({(0, 1), (T - 1, 1), (0, T)}):
+        pr, orc_f, saved, dy, dh = _bwd_inputs_from_oracle_fwd(w, j, nsh, inp, grads)
+        d = _desc(w, j, nsh)
+        out = ops.backward(d, dy, dh, saved["h"], inp["gamma"], saved["mask"] if p > 0 else None,
+                           saved["rstd"], saved["mean"] if nm == "ln" else None)
+        torch.cuda.synchronize()
+        _check_bwd(w, pr, orc_f["h"], _np(dy), _np(dh), _np(inp["gamma"]),
+                   orc_f["mask"] if p > 0 else None, out)
+
+
+def test_bwd_empty_rows_zeroes_dgamma():
+    w = syn.WORKLOADS["gpt_ln_bf16"].with_(S=0)
+    d = _desc(w, 0)
+    z = torch.empty((0, w.H), device=DEV, dtype=torch.bfloat16)
+    g = torch.ones(w.H, device=DEV, dtype=torch.bfloat16)
+    dg = torch.full((w.H,), 7.0, device=DEV)
+    dbt = torch.full((w.H,), 7.0, device=DEV)
+    ws = ops.workspace_for(d, DEV)
+    ops.sp_rs_dropout_residual_norm_bwd(d, z, None, z, g, torch.empty((0, w.H), device=DEV,
+                                        dtype=torch.uint8), torch.empty(0, device=DEV),
+                                        torch.empty(0, device=DEV), z, z, dg, dbt, ws)
+    torch.cuda.synchronize()
+    assert torch.all(dg == 0) and torch.all(dbt == 0)
+
+
+def test_bwd_workspace_too_small_is_rejected():
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    d = _desc(w, 0)
+    need = ops.sp_rs_bwd_workspace_bytes(d)
+    assert need > 0
+    t = torch.zeros((w.R, w.H), device=DEV, dtype=torch.bfloat16)
+    m = torch.zeros((w.R, w.H), device=DEV, dtype=torch.uint8)
+    r = torch.ones(w.R, device=DEV)
+    g = torch.ones(w.H, device=DEV, dtype=torch.bfloat16)
+    dg = torch.empty(w.H, device=DEV)
+    ws = torch.empty(need - 16, device=DEV, dtype=torch.uint8)
+    with pytest.raises(RuntimeError, match="WORKSPACE"):
+        ops.sp_rs_dropout_residual_norm_bwd(d, t, None, t, g, m, r, None, t.clone(), t.clone(), dg,
+                                            None, ws)
+
+
+# ---------------------------------------------------------------------------
+# layout transforms
+# ---------------------------------------------------------------------------
+
+def test_layout_full_size_bit_exact_and_roundtrip():
+    lw = syn.LAYOUT
+    x = syn.layout_input(lw, DEV)
+    hp = ops.sp2hp_out(x, lw.T)
+    back = ops.hp2sp_out(hp)
+    torch.cuda.synchronize()
+    xn = _np(x)
+    assert np.array_equal(_np(hp), oracle.sp2hp(xn, lw.T))
+    assert torch.equal(back, x)
+    y = syn.layout_input(lw, DEV, seed=5).view(lw.T, lw.N, lw.H // lw.T)
+    assert np.array_equal(_np(ops.hp2sp_out(y)), oracle.hp2sp(_np(y)))
+
+
+@pytest.mark.parametrize("T,N,H,dt", [(1, 4, 8, "bf16"), (3, 9, 24, "bf16"), (8, 64, 512, "bf16"),
+                                      (2, 6, 8, "f32"), (4, 12, 48, "f32"), (3, 300, 2064, "bf16")])
+def test_layout_edge_shapes(T, N, H, dt):
+    lw = syn.LayoutWorkload("edge", T, N, H, dt, 1.0, 77)
+    x = syn.layout_input(lw, DEV)
+    hp = ops.sp2hp_out(x, T)
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(hp), oracle.sp2hp_all_to_all(_np(x), T))
+    assert torch.equal(ops.hp2sp_out(hp), x)
+
+
+# ---------------------------------------------------------------------------
+# determinism, guard zones, streams
+# ---------------------------------------------------------------------------
+
+def test_bitwise_deterministic_runs():
+    w = syn.WORKLOADS["gpt_ln_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    d = _desc(w, 0, w.T)
+    outs = []
+    for _ in range(2):
+        f = ops.forward(d, inp["partials"], inp["residual"].view(-1, w.H), inp["gamma"], inp["beta"])
+        b = ops.backward(d, grads["dy"].view(-1, w.H), grads["dh_out"].view(-1, w.H), f["h"],
+                         inp["gamma"], f["mask"], f["rstd"], f["mean"])
+        outs.append({**f, **b})
+    torch.cuda.synchronize()
+    for k, v in outs[0].items():
+        if v is not None:
+            assert torch.equal(v, outs[1][k]), k
+
+
+def test_outputs_stay_inside_their_buffers():
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    R, H, PAD = w.R, w.H, 4096
+    d = _desc(w, 1)
+
+    def guarded(n, dtype):
+        buf = torch.full((n + 2 * PAD,), 0x5A if dtype == torch.uint8 else 3.0, device=DEV, dtype=dtype)
+        return buf, buf[PAD:PAD + n]
+
+    hb, h = guarded(R * H, torch.bfloat16)
+    yb, y = guarded(R * H, torch.bfloat16)
+    mb, m = guarded(R * H, torch.uint8)
+    rb, r = guarded(R, torch.float32)
+    ops.sp_rs_dropout_residual_norm_fwd(d, inp["partials"], inp["residual"].view(-1, H)[R:2 * R],
+                                        inp["gamma"], None, h, y, m, r, None)
+    grads = syn.upstream_grads(w, DEV)
+    drb, dres = guarded(R * H, torch.bfloat16)
+    dsb, dsum = guarded(R * H, torch.bfloat16)
+    dgb, dg = guarded(H, torch.float32)
+    ops.sp_rs_dropout_residual_norm_bwd(d, grads["dy"].view(-1, H)[R:2 * R], None, h, inp["gamma"], m,
+                                        r, None, dres, dsum, dg, None, ops.workspace_for(d, DEV))
+    torch.cuda.synchronize()
+    for buf in [hb, yb, mb, rb, drb, dsb, dgb]:
+        fill = 0x5A if buf.dtype == torch.uint8 else 3.0
+        assert torch.all(buf[:PAD] == fill) and torch.all(buf[-PAD:] == fill)
+
+
+def test_side_stream_matches_default_stream():
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    d = _desc(w, 0, 2)
+    ref = ops.forward(d, inp["partials"], inp["residual"].view(-1, w.H), inp["gamma"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        got = ops.forward(d, inp["partials"], inp["residual"].view(-1, w.H), inp["gamma"])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for k in ["h", "y", "mask", "rstd"]:
+        assert torch.equal(ref[k], got[k])
