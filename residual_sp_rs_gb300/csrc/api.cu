@@ -166,7 +166,9 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   a.thr = (uint32_t)std::floor((double)desc->p * 4294967296.0);
   a.key0 = (uint32_t)desc->seed;
   a.key1 = (uint32_t)(desc->seed >> 32);
-  a.scale = (float)(1.0 / (1.0 - (double)desc->p));
+  const double scale = 1.0 / (1.0 - (double)desc->p);
+  a.scale = (float)scale;
+  a.scale_lo = (float)(scale - (double)a.scale);
   a.eps = desc->eps;
   a.Hf = (float)pr.H;
   a.dropout = desc->p > 0.0f ? 1 : 0;

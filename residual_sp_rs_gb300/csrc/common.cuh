@@ -123,6 +123,38 @@ struct Act16<__nv_bfloat16> {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Residual stream value h = res + acc * s, rounded ONCE to bf16 from (almost)
+// the exact value.  s = s_hi + s_lo carries 1/(1-p) to ~48 bits.  The product
+// and the sum are formed with error-free transformations (Dekker's product
+// via fma, Knuth's TwoSum), giving h = h_hi + err exactly up to the s_lo term.
+// Rounding h_hi to nearest-even bf16 is then correct except when h_hi sits
+// exactly on a bf16 midpoint; there the sign of err decides.  Such midpoints
+// are common: when the partial sum times 1/(1-p) is (nearly) dyadic, fp32
+// arithmetic lands exactly on the tie that the exact value misses.
+// Returns the bf16 bit pattern.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t residual_bf16(float res, float acc, float s_hi, float s_lo,
+                                                  bool keep) {
+  float h_hi = res, err = 0.f;
+  if (keep) {
+    const float z_hi = __fmul_rn(acc, s_hi);
+    const float z_lo = __fadd_rn(__fmaf_rn(acc, s_hi, -z_hi), __fmul_rn(acc, s_lo));
+    h_hi = __fadd_rn(res, z_hi);
+    const float bb = __fsub_rn(h_hi, res);
+    const float e1 = __fadd_rn(__fsub_rn(res, __fsub_rn(h_hi, bb)), __fsub_rn(z_hi, bb));
+    err = __fadd_rn(e1, z_lo);
+  }
+  const uint32_t u = __float_as_uint(h_hi);
+  if ((u & 0xFFFFu) == 0x8000u && err != 0.f) {
+    // exact value is past the midpoint (away from zero) when err has h's sign
+    const bool away = (err > 0.f) == (h_hi > 0.f);
+    return (u >> 16) + (away ? 1u : 0u);
+  }
+  const __nv_bfloat16 b = __float2bfloat16_rn(h_hi);
+  return (uint32_t) * reinterpret_cast<const unsigned short*>(&b);
+}
+
 // Store EV mask bytes (bit e of `bits` -> byte e).
 template <int EV>
 __device__ __forceinline__ void st_mask(uint8_t* p, uint32_t bits);
@@ -221,7 +253,8 @@ struct FwdArgs {
   int32_t tpr;           // threads per row (multiple of 32)
   uint32_t thr;          // keep threshold floor(p * 2^32)
   uint32_t key0, key1;   // Philox key (seed)
-  float scale;           // 1 / (1 - p)
+  float scale;           // 1 / (1 - p), rounded to fp32
+  float scale_lo;        // 1 / (1 - p) - scale, rounded to fp32
   float eps;
   float Hf;              // H as float
   int32_t dropout;       // p > 0

@@ -75,10 +75,20 @@ __global__ void __launch_bounds__(512) sp_fwd_kernel(const FwdArgs a) {
         keep = keep_bits4(g0 >> 2, a.key0, a.key1, a.thr);
         if constexpr (EV == 8) keep |= keep_bits4((g0 >> 2) + 1, a.key0, a.key1, a.thr) << 4;
       }
-      float hv[EV];
+      uint4 hp;
+      if constexpr (EV == 8) {
+        uint32_t hb[EV];
 #pragma unroll
-      for (int e = 0; e < EV; ++e) hv[e] = rs[e] + (((keep >> e) & 1u) ? acc[e] * a.scale : 0.f);
-      const uint4 hp = V::pack(hv);
+        for (int e = 0; e < EV; ++e)
+          hb[e] = residual_bf16(rs[e], acc[e], a.scale, a.scale_lo, (keep >> e) & 1u);
+        hp = make_uint4(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16), hb[4] | (hb[5] << 16),
+                        hb[6] | (hb[7] << 16));
+      } else {
+        float hv[EV];
+#pragma unroll
+        for (int e = 0; e < EV; ++e) hv[e] = rs[e] + (((keep >> e) & 1u) ? acc[e] * a.scale : 0.f);
+        hp = V::pack(hv);
+      }
       st_stream(reinterpret_cast<Act*>(a.h) + r * (int64_t)a.H + (int64_t)v * EV, hp);
       if (a.mask) st_mask<EV>(a.mask + r * (int64_t)a.H + (int64_t)v * EV, keep);
       V::unpack(hp, hr[k]);  // the norm reads the stored (rounded) value

@@ -7,9 +7,11 @@ Tolerances (stated for the SP-region hot path, derived from its arithmetic):
     far below the other 1/2 ulp), with an absolute floor of 2^-16 * max|row|
     for elements that cancel to near zero (where fp32 rounding of the terms,
     not the final rounding, dominates).
-  * y additionally allows |gamma * rstd| * |h_gpu - h_oracle| where the two
-    stored residual-stream values differ: an fp32-vs-f64 rounding flip of the
-    stored h (at most 1 ulp, checked separately) is read by the norm.
+  * the stored residual stream h is rounded once from (almost) the exact
+    value on both sides, so the two agree bit for bit except in vanishingly
+    rare cases (at most 1e-5 of the elements, checked); where they differ,
+    y additionally allows the first-order effect of that difference on the
+    element and on its row's mean and rstd.
   * fp32 outputs: |gpu - exact| <= 1e-5 * max(|exact|, rms(row)).
   * rstd: relative 1e-5 plus the first-order effect of h flips on the row's
     second moment.
@@ -90,26 +92,33 @@ def compare_fwd(dtype: str, norm: str, gpu: dict, orc: dict, gamma_f64: np.ndarr
     orc: oracle outputs for the same rows."""
     assert np.array_equal(gpu["mask"], orc["mask"]), "mask differs"
     check_act("h", dtype, gpu["h"], orc["h_exact"])
-    h_gpu = oracle.to_f64(gpu["h"], dtype).reshape(orc["h_exact"].shape)
-    h_or = oracle.to_f64(orc["h"], dtype).reshape(orc["h_exact"].shape)
+    shape = orc["h_exact"].shape
+    H = shape[-1]
+    h_gpu = oracle.to_f64(gpu["h"], dtype).reshape(shape)
+    h_or = oracle.to_f64(orc["h"], dtype).reshape(shape)
     dh = np.abs(h_gpu - h_or)
-    rstd = orc["rstd"][:, None]
-    extra = np.abs(gamma_f64)[None, :] * rstd * dh if dtype == "bf16" else None
-    check_act("y", dtype, gpu["y"], orc["y_exact"], extra)
-    # rstd: first-order effect of flipped h on the row's second moment
-    if norm == "ln":
-        cen = np.abs(h_or - orc["mean"][:, None])
-    else:
-        cen = np.abs(h_or)
-    H = h_or.shape[-1]
+    if dtype == "bf16":
+        # the kernel rounds h once from (almost) the exact value: flips of the
+        # stored residual stream must be vanishingly rare
+        flips = int((dh > 0).sum())
+        assert flips <= max(2, int(1e-5 * dh.size)), f"h: {flips} rounding flips"
+    r = orc["rstd"][:, None]
+    mu = orc["mean"][:, None] if norm == "ln" else 0.0
+    xhat = (h_or - mu) * r
     second = (1.0 / orc["rstd"]) ** 2
-    flip_rel = (cen * dh).sum(-1) / (H * second)
+    # first-order effect of any flipped h on the row statistics
+    flip_rel = (np.abs(h_or - mu) * dh).sum(-1) / (H * second)
+    dmu = dh.sum(-1) / H if norm == "ln" else np.zeros(len(second))
+    extra = None
+    if dtype == "bf16":
+        g = np.abs(gamma_f64)[None, :]
+        extra = g * r * (dh + dmu[:, None]) + 2 * g * np.abs(xhat) * flip_rel[:, None]
+    check_act("y", dtype, gpu["y"], orc["y_exact"], extra)
     r_gpu = np.asarray(gpu["rstd"], dtype=np.float64)
     bad = np.abs(r_gpu - orc["rstd"]) > (1e-5 + 2 * flip_rel) * orc["rstd"]
     assert not bad.any(), f"rstd: {bad.sum()} rows out of tolerance"
     if norm == "ln":
         m_gpu = np.asarray(gpu["mean"], dtype=np.float64)
-        rms = np.sqrt(second)
-        tolm = 1e-5 * np.maximum(np.abs(orc["mean"]), rms) + dh.sum(-1) / H
+        tolm = 1e-5 * np.maximum(np.abs(orc["mean"]), np.sqrt(second)) + dmu
         bad = np.abs(m_gpu - orc["mean"]) > tolm
         assert not bad.any(), f"mean: {bad.sum()} rows out of tolerance"
