@@ -127,11 +127,12 @@ struct Act16<__nv_bfloat16> {
 // Residual stream value h = res + acc * s, rounded ONCE to bf16 from (almost)
 // the exact value.  s = s_hi + s_lo carries 1/(1-p) to ~48 bits.  The product
 // and the sum are formed with error-free transformations (Dekker's product
-// via fma, Knuth's TwoSum), giving h = h_hi + err exactly up to the s_lo term.
-// Rounding h_hi to nearest-even bf16 is then correct except when h_hi sits
-// exactly on a bf16 midpoint; there the sign of err decides.  Such midpoints
-// are common: when the partial sum times 1/(1-p) is (nearly) dyadic, fp32
-// arithmetic lands exactly on the tie that the exact value misses.
+// via fma, Knuth's TwoSum), so h = h_hi + err up to the tiny acc*s_lo
+// rounding.  The bf16 result is the nearest-even rounding of h_hi + err: the
+// magnitude is compared with the bf16 midpoint above trunc(h_hi).  Rounding
+// h_hi alone would be wrong whenever the exact value and h_hi straddle a
+// midpoint, which is common: when the partial sum times 1/(1-p) is (nearly)
+// dyadic, fp32 arithmetic lands on or next to a tie the exact value misses.
 // Returns the bf16 bit pattern.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t residual_bf16(float res, float acc, float s_hi, float s_lo,
@@ -145,14 +146,23 @@ __device__ __forceinline__ uint32_t residual_bf16(float res, float acc, float s_
     const float e1 = __fadd_rn(__fsub_rn(res, __fsub_rn(h_hi, bb)), __fsub_rn(z_hi, bb));
     err = __fadd_rn(e1, z_lo);
   }
-  const uint32_t u = __float_as_uint(h_hi);
-  if ((u & 0xFFFFu) == 0x8000u && err != 0.f) {
-    // exact value is past the midpoint (away from zero) when err has h's sign
-    const bool away = (err > 0.f) == (h_hi > 0.f);
-    return (u >> 16) + (away ? 1u : 0u);
+  // renormalise (TwoSum): hs = fl(h_hi + err), |lo| <= ulp(hs)/2, so the
+  // midpoint test below also holds when res and z cancel
+  const float hs = __fadd_rn(h_hi, err);
+  const float bs = __fsub_rn(hs, h_hi);
+  const float lo = __fadd_rn(__fsub_rn(h_hi, __fsub_rn(hs, bs)), __fsub_rn(err, bs));
+  const uint32_t u = __float_as_uint(hs);
+  if ((u & 0x7FFFFFFFu) == 0u) {  // exact cancellation: the value is lo itself
+    const __nv_bfloat16 b = __float2bfloat16_rn(lo);
+    return (uint32_t) * reinterpret_cast<const unsigned short*>(&b);
   }
-  const __nv_bfloat16 b = __float2bfloat16_rn(h_hi);
-  return (uint32_t) * reinterpret_cast<const unsigned short*>(&b);
+  const uint32_t trunc = u & 0xFFFF0000u;              // toward zero, same exponent
+  const float mid = __uint_as_float(trunc | 0x8000u);  // midpoint above |trunc|
+  // |h| - |mid|: the first difference is exact (same binade), lo adds the rest
+  const float d = __fadd_rn(__fsub_rn(fabsf(hs), fabsf(mid)), hs > 0.f ? lo : -lo);
+  uint32_t b = trunc >> 16;
+  if (d > 0.f || (d == 0.f && (b & 1u))) b += 1u;
+  return b;
 }
 
 // Store EV mask bytes (bit e of `bits` -> byte e).
