@@ -154,6 +154,43 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc,
                                             void* workspace, size_t workspace_bytes,
                                             sp_stream_t stream);
 
+/* Size of the fixed device scratch of sp_rs_dropout_residual_norm_bwd_noalloc. */
+#define SP_NOALLOC_SCRATCH_BYTES (2u << 20)
+
+/* The backward above without a workspace argument.  The pages have no
+ * counterpart to this entry point; it is here for callers that cannot
+ * allocate device memory at the point where they run the backward: code
+ * inside an allocator callback or an out-of-memory handler (allocating there
+ * would re-enter the allocator), frameworks whose caching allocator already
+ * holds the device memory and must not see cudaMalloc called behind its
+ * back, and latency-critical paths that avoid cudaMalloc / cudaFree because
+ * those calls can synchronise the device.
+ *
+ * Instead of `workspace`, the call uses a fixed array of
+ * SP_NOALLOC_SCRATCH_BYTES (2 MiB) in the library's own device memory; every
+ * GPU that loads the library reserves it until the process exits.  Arguments,
+ * results and errors are those of sp_rs_dropout_residual_norm_bwd, except that
+ * a problem whose dgamma/dbeta partial rows need more than
+ * SP_NOALLOC_SCRATCH_BYTES (sp_rs_bwd_workspace_bytes(desc) larger than it)
+ * is refused with SP_ERR_WORKSPACE before anything is launched.  The call
+ * itself allocates nothing.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture begins.  All calls share the one array, which keeps whatever the
+ * previous call left in it; nothing in it has to start at zero, because each
+ * call writes every partial row it later reads.  Calls whose kernels can
+ * overlap on the GPU (different streams, or host threads without ordering)
+ * race on the array: order them on one stream. */
+sp_status_t sp_rs_dropout_residual_norm_bwd_noalloc(const sp_rs_desc_t* desc,
+                                                    const void* dy, const void* dh_out,
+                                                    const void* h_saved, const void* gamma,
+                                                    const uint8_t* mask,
+                                                    const float* rstd, const float* mean,
+                                                    void* d_residual, void* d_sum,
+                                                    float* dgamma, float* dbeta,
+                                                    sp_stream_t stream);
+
 /* sp2hp ([ATL] §5): sequence-split -> hidden-split.  `in` is [N, H]: the T
  * rank shards [N/T, H] stacked in rank order; `out` is [T][N][H/T] where
  * out[r] is what rank r holds after the all-to-all:
