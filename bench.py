@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--seq", type=int, default=None,
+                    help="override S (smaller captures of the same kernels for ncu)")
     return ap.parse_args()
 
 
@@ -156,6 +158,8 @@ def run_ours(args):
     ops.lib()
 
     w = syn.WORKLOADS[args.workload]
+    if args.seq:
+        w = w.with_(S=args.seq)
     T, H = w.T, w.H
     rows = w.S * w.B
     tdt = syn.torch_dtype(w.dtype)
@@ -250,26 +254,29 @@ def run_ours(args):
     step_bytes = fwd_bytes(w, rows) + bwd_bytes(w, rows) + 2 * layout_bytes(w, rows)
     step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
 
-    # ---- per-launch durations of the main kernels (events on the launch stream)
-    def time_launches(fn, iters):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(iters)]
-        for i in range(iters):
-            s = sets[i % n_sets]
-            evs[i][0].record()
-            fn(s)
-            evs[i][1].record()
+    # ---- per-launch durations of the main kernels: each kernel alone, launched
+    # back to back from one CUDA graph over the rotating sets, CUDA events
+    # around the replays on the launching stream
+    def time_launches(fn, reps):
+        per_graph = 4 * n_sets
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="relaxed"):
+            for i in range(per_graph):
+                fn(sets[i % n_sets])
+        g.replay()
         torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in evs) / iters
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * per_graph)
 
-    for s in sets:
-        fwd(s)
-        bwd(s)
-    torch.cuda.synchronize()
-    t_fwd = time_launches(fwd, args.roofline_iters)
-    t_bwd = time_launches(bwd, args.roofline_iters)
-    t_sp2hp = time_launches(lambda s: ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype),
-                            args.roofline_iters)
+    reps = max(1, args.roofline_iters // (4 * n_sets))
+    t_fwd = time_launches(fwd, reps)
+    t_bwd = time_launches(bwd, reps)
+    t_sp2hp = time_launches(lambda s: ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype), reps)
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))

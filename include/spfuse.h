@@ -155,7 +155,7 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc,
                                             sp_stream_t stream);
 
 /* Size of the fixed device scratch of sp_rs_dropout_residual_norm_bwd_noalloc. */
-#define SP_NOALLOC_SCRATCH_BYTES (2u << 20)
+#define SP_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* The backward above without a workspace argument.  The pages have no
  * counterpart to this entry point; it is here for callers that cannot
@@ -167,7 +167,7 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc,
  * those calls can synchronise the device.
  *
  * Instead of `workspace`, the call uses a fixed array of
- * SP_NOALLOC_SCRATCH_BYTES (2 MiB) in the library's own device memory; every
+ * SP_NOALLOC_SCRATCH_BYTES (8 MiB) in the library's own device memory; every
  * GPU that loads the library reserves it until the process exits.  Arguments,
  * results and errors are those of sp_rs_dropout_residual_norm_bwd, except that
  * a problem whose dgamma/dbeta partial rows need more than

@@ -82,32 +82,53 @@ RowShape row_shape(int nvec, int vpt_cap) {
   return s;
 }
 
-RowShape bwd_row_shape(const Problem& pr) { return row_shape(pr.nvec, pr.ev == 8 ? 2 : 4); }
+RowShape bwd_row_shape(const Problem& pr) { return row_shape(pr.nvec, pr.ev == 8 ? 3 : 4); }
 
 struct BwdPlan {
+  bool tma;    // TMA-fed kernel (else the register kernel with cluster partials)
+  BwdTmaPlan tp;
   RowShape shape;
   size_t smem;
   int64_t rows_per_cta;
-  int ctas;    // multiple of the cluster size
-  int nparts;  // partial rows per statistic (clusters)
+  int ctas;    // register kernel: a multiple of the cluster size
+  int nparts;  // partial rows per statistic (CTAs or clusters)
   size_t ws_bytes;
 };
 
-sp_status_t plan_bwd(const Problem& pr, BwdPlan* pl) {
+// has_dh / has_mask only shape the TMA ring; the choice of kernel and the
+// workspace size are decided with both present, so the workspace query and
+// the call always agree.
+sp_status_t plan_bwd(const Problem& pr, bool has_dh, bool has_mask, BwdPlan* pl) {
   const bool ln = pr.norm == SP_LAYERNORM;
+  pl->tma = false;
+  if (pr.dtype == SP_BF16) {
+    int dev = 0, sms = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return SP_ERR_CUDA;
+    BwdTmaPlan probe;
+    if (plan_bwd_tma(pr.H, ln, true, true, optin, &probe)) {
+      pl->tma = true;
+      plan_bwd_tma(pr.H, ln, has_dh, has_mask, optin, &pl->tp);
+      const int64_t ctas = pr.rows < sms ? (pr.rows > 0 ? pr.rows : 1) : sms;
+      pl->rows_per_cta = pr.rows > 0 ? (pr.rows + ctas - 1) / ctas : 1;
+      pl->ctas = pr.rows > 0 ? (int)((pr.rows + pl->rows_per_cta - 1) / pl->rows_per_cta) : 0;
+      pl->nparts = pl->ctas;
+      pl->ws_bytes = (size_t)(ctas > 0 ? ctas : 1) * (size_t)pr.H * sizeof(float) * (ln ? 2 : 1);
+      return SP_OK;
+    }
+  }
   pl->shape = bwd_row_shape(pr);
-  pl->smem = (size_t)(ln ? 2 : 1) * (size_t)pr.H * sizeof(float);
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SP_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return SP_ERR_CUDA;
-  int per_sm = bwd_ctas_per_sm(pr.dtype, ln, pl->shape, pl->smem);
-  if (per_sm < 1) return SP_ERR_CUDA;
+  // CTA column sums, then the gamma vectors
+  pl->smem = (size_t)(ln ? 2 : 1) * (size_t)pr.H * sizeof(float) + (size_t)pr.nvec * 16;
+  const int clusters = bwd_max_active_clusters(pr.dtype, ln, pl->shape, pl->smem);
+  if (clusters < 1) return SP_ERR_CUDA;
   const int cluster = 8;
   const int rpc = pl->shape.block / pl->shape.tpr;
-  // as many CTAs as fit at once, but at least one row per row group
+  // as many CTAs as are resident at once, but at least one row per row group
   int64_t want = (pr.rows + rpc - 1) / rpc;
-  int64_t cap = (int64_t)sms * per_sm;
+  int64_t cap = (int64_t)clusters * cluster;
   int64_t ctas = want < cap ? want : cap;
   ctas = ((ctas + cluster - 1) / cluster) * cluster;
   if (ctas < cluster) ctas = cluster;
@@ -164,8 +185,11 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   a.H = (int32_t)pr.H;
   a.nvec = pr.nvec;
   a.thr = (uint32_t)std::floor((double)desc->p * 4294967296.0);
-  a.key0 = (uint32_t)desc->seed;
-  a.key1 = (uint32_t)(desc->seed >> 32);
+  // Philox round keys: the seed's two words advanced by the Weyl increments
+  for (int i = 0; i < 10; ++i) {
+    a.keys.rk[2 * i] = (uint32_t)desc->seed + (uint32_t)i * 0x9E3779B9u;
+    a.keys.rk[2 * i + 1] = (uint32_t)(desc->seed >> 32) + (uint32_t)i * 0xBB67AE85u;
+  }
   const double scale = 1.0 / (1.0 - (double)desc->p);
   a.scale = (float)scale;
   a.scale_lo = (float)(scale - (double)a.scale);
@@ -191,7 +215,7 @@ size_t sp_rs_bwd_workspace_bytes(const sp_rs_desc_t* desc) {
   Problem pr;
   if (check_desc(desc, &pr) != SP_OK) return 0;
   BwdPlan pl;
-  if (plan_bwd(pr, &pl) != SP_OK) return 0;
+  if (plan_bwd(pr, true, true, &pl) != SP_OK) return 0;
   return pl.ws_bytes;
 }
 
@@ -219,7 +243,7 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc, const void
       !aligned(dgamma, 16) || (ln && !aligned(dbeta, 16)))
     return SP_ERR_ALIGN;
   BwdPlan pl;
-  st = plan_bwd(pr, &pl);
+  st = plan_bwd(pr, dh_out != nullptr, desc->p > 0.0f, &pl);
   if (st != SP_OK) return st;
   if (!workspace || workspace_bytes < pl.ws_bytes) return SP_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return SP_ERR_ALIGN;
@@ -248,7 +272,13 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc, const void
     a.nparts = pl.nparts;
     a.scale = (float)(1.0 / (1.0 - (double)desc->p));
     a.Hf = (float)pr.H;
-    cudaError_t e = launch_bwd(pr.dtype, ln, a, pl.shape, dim3((unsigned)pl.ctas), pl.smem, cs);
+    cudaError_t e;
+    if (pl.tma) {
+      a.tpr = pl.tp.shape.tpr;
+      e = launch_bwd_tma(ln, a, pl.tp, dim3((unsigned)pl.ctas), cs);
+    } else {
+      e = launch_bwd(pr.dtype, ln, a, pl.shape, dim3((unsigned)pl.ctas), pl.smem, cs);
+    }
     if (e != cudaSuccess) return SP_ERR_CUDA;
     nparts = pl.nparts;
   }

@@ -24,14 +24,21 @@ void (*bwd_kernel(int dtype, bool ln, int vpt))(const BwdArgs) {
 
 }  // namespace
 
-int bwd_ctas_per_sm(int dtype, bool ln, const RowShape& s, size_t smem) {
+// How many 8-CTA clusters of the backward kernel can be resident at once on
+// the current device (clusters must fit inside one GPC, so this is at most,
+// and often below, SMs * CTAs-per-SM / 8).
+int bwd_max_active_clusters(int dtype, bool ln, const RowShape& s, size_t smem) {
   void (*k)(const BwdArgs) = bwd_kernel(dtype, ln, s.vpt);
   if (!k) return 0;
-  if (smem > 48 * 1024 &&
+  if (smem > kSmemOptInThreshold &&
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kBwdCluster * 64);
+  cfg.blockDim = dim3(s.block);
+  cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, s.block, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (const void*)k, &cfg) != cudaSuccess) return 0;
   return n;
 }
 
@@ -39,7 +46,7 @@ cudaError_t launch_bwd(int dtype, bool ln, const BwdArgs& a, const RowShape& s, 
                        size_t smem, cudaStream_t st) {
   void (*k)(const BwdArgs) = bwd_kernel(dtype, ln, s.vpt);
   if (!k) return cudaErrorInvalidValue;
-  if (smem > 48 * 1024) {
+  if (smem > kSmemOptInThreshold) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }

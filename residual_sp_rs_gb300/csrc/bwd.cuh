@@ -22,6 +22,12 @@ namespace cg = cooperative_groups;
 
 constexpr int kBwdCluster = 8;  // CTAs per thread-block cluster in the backward
 
+// The compiler must not keep unpacked copies of these registers alive across
+// the row reduction; re-unpacking after it is cheaper than the registers.
+__device__ __forceinline__ void opaque(uint4& v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+}
+
 template <typename Act, bool LN, int VPT>
 __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
     sp_bwd_kernel(const BwdArgs a) {
@@ -29,7 +35,8 @@ __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
   constexpr int EV = V::EV;
   constexpr int NS = LN ? 2 : 1;  // row sums needed: mean(g*xhat) (+ mean(g))
   __shared__ float red[2 * 32 * 2];
-  extern __shared__ float colacc[];  // [NS][H] CTA column sums
+  extern __shared__ float colacc[];  // [NS][H] CTA column sums, then gamma vectors [nvec]
+  uint4* sgam = reinterpret_cast<uint4*>(colacc + NS * a.H);
 
   const int tpr = a.tpr;
   const int rg = threadIdx.x / tpr;
@@ -41,19 +48,19 @@ __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
   grid_dep_wait();
   grid_dep_launch_dependents();
 
-  float gm[VPT][EV];
+  for (int i = threadIdx.x; i < a.nvec; i += blockDim.x)
+    sgam[i] = ld_cached(reinterpret_cast<const Act*>(a.gamma) + i * EV);
+  __syncthreads();
+
   float dg[VPT][EV];
   float db[LN ? VPT : 1][EV];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
-    const int v = lr + k * tpr;
 #pragma unroll
     for (int e = 0; e < EV; ++e) {
-      gm[k][e] = 0.f;
       dg[k][e] = 0.f;
       if constexpr (LN) db[k][e] = 0.f;
     }
-    if (v < a.nvec) V::unpack(ld_cached(reinterpret_cast<const Act*>(a.gamma) + v * EV), gm[k]);
   }
 
   float* rred = red + rg * 2 * (tpr >> 5) * NS;
@@ -69,34 +76,28 @@ __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
         const int64_t o = ro + (int64_t)v * EV;
         dyv[k] = ld_stream(reinterpret_cast<const Act*>(a.dy) + o);
         hv[k] = ld_stream(reinterpret_cast<const Act*>(a.h) + o);
-        if (a.dh) dhv[k] = ld_stream(reinterpret_cast<const Act*>(a.dh) + o);
+        dhv[k] = a.dh ? ld_stream(reinterpret_cast<const Act*>(a.dh) + o) : make_uint4(0u, 0u, 0u, 0u);
         mk[k] = a.mask ? ld_mask<EV>(a.mask + o) : (1u << EV) - 1u;
       }
     }
     const float rstd = __ldcs(a.rstd + r);
     const float mu = LN ? __ldcs(a.mean + r) : 0.f;
 
-    float xh[VPT][EV], dyf[VPT][EV];
+    // pass 1: the row sums of g*xhat (and g)
     float sums[NS];
 #pragma unroll
     for (int i = 0; i < NS; ++i) sums[i] = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      const int v = lr + k * tpr;
-#pragma unroll
-      for (int e = 0; e < EV; ++e) {
-        xh[k][e] = 0.f;
-        dyf[k][e] = 0.f;
-      }
-      if (v < a.nvec) {
-        float hf[EV];
-        V::unpack(dyv[k], dyf[k]);
+      if (lr + k * tpr < a.nvec) {
+        float dyf[EV], hf[EV], gm[EV];
+        V::unpack(dyv[k], dyf);
         V::unpack(hv[k], hf);
+        V::unpack(sgam[lr + k * tpr], gm);
 #pragma unroll
         for (int e = 0; e < EV; ++e) {
-          xh[k][e] = (hf[e] - mu) * rstd;
-          const float g = gm[k][e] * dyf[k][e];
-          sums[0] += g * xh[k][e];
+          const float g = gm[e] * dyf[e];
+          sums[0] += g * ((hf[e] - mu) * rstd);
           if constexpr (LN) sums[1] += g;
         }
       }
@@ -106,25 +107,26 @@ __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
     const float c_gx = sums[0] / a.Hf;
     const float c_g = LN ? sums[NS - 1] / a.Hf : 0.f;
 
+    // pass 2: input gradients, mask-gated gradient of the partials, dgamma/dbeta
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lr + k * tpr;
       if (v < a.nvec) {
-        float dhf[EV], dres[EV], dsum[EV];
-        if (a.dh) {
-          V::unpack(dhv[k], dhf);
-        } else {
-#pragma unroll
-          for (int e = 0; e < EV; ++e) dhf[e] = 0.f;
-        }
+        opaque(dyv[k]);
+        opaque(hv[k]);
+        float dyf[EV], hf[EV], gm[EV], dhf[EV], dres[EV], dsum[EV];
+        V::unpack(dyv[k], dyf);
+        V::unpack(hv[k], hf);
+        V::unpack(dhv[k], dhf);
+        V::unpack(sgam[v], gm);
 #pragma unroll
         for (int e = 0; e < EV; ++e) {
-          const float g = gm[k][e] * dyf[k][e];
-          const float dHn = rstd * (g - c_g - xh[k][e] * c_gx);
-          dres[e] = dHn + dhf[e];
+          const float xh = (hf[e] - mu) * rstd;
+          const float g = gm[e] * dyf[e];
+          dres[e] = rstd * (g - c_g - xh * c_gx) + dhf[e];
           dsum[e] = ((mk[k] >> e) & 1u) ? dres[e] * a.scale : 0.f;
-          dg[k][e] += dyf[k][e] * xh[k][e];
-          if constexpr (LN) db[k][e] += dyf[k][e];
+          dg[k][e] += dyf[e] * xh;
+          if constexpr (LN) db[k][e] += dyf[e];
         }
         const int64_t o = ro + (int64_t)v * EV;
         st_stream(reinterpret_cast<Act*>(a.d_res) + o, V::pack(dres));

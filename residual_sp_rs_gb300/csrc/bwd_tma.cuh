@@ -1,0 +1,238 @@
+// bwd_tma.cuh -- backward of the SP region, rows streamed through shared
+// memory by the Tensor Memory Accelerator (bulk copies + mbarriers).
+//
+// One persistent CTA per SM owns a contiguous block of token rows.  A
+// producer warp keeps a ring of NST one-row stages full: for each row it
+// issues one bulk copy per input tensor (dy, h, dh_out, mask) on the stage's
+// "full" mbarrier.  Consumer row groups (tpr threads each) take rows
+// round-robin, compute from shared memory and release the stage on its
+// "empty" mbarrier.  The loads of up to NST rows are in flight at all times,
+// without holding them in registers, so the HBM pipe stays busy through the
+// row reductions and the stores.  dgamma/dbeta accumulate in registers per
+// thread-owned column; at the end the CTA adds its row groups in order and
+// writes one fp32 partial row, which sp_colsum_kernel reduces in CTA order.
+//
+// If a wait times out (a copy that never lands), the CTA stops, waits (with a
+// limit) for what it issued, and poisons its dgamma/dbeta partial with NaN so
+// the failure is visible in the result.
+#pragma once
+
+#include "common.cuh"
+#include "tma.cuh"
+
+namespace spf {
+
+template <bool LN, int VPT>
+__global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
+  using V = Act16<__nv_bfloat16>;
+  constexpr int EV = 8;
+  constexpr int NS = LN ? 2 : 1;
+  __shared__ float red[2 * 32 * 2];
+  __shared__ int s_failed;  // set when any wait timed out
+  extern __shared__ __align__(16) unsigned char dsm[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
+  uint64_t* empty = full + L.nst;
+  float* colacc = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // [NS][H]
+  uint4* sgam = reinterpret_cast<uint4*>(colacc + NS * a.H);                          // [nvec]
+  unsigned char* stages = dsm + L.smem_stages;
+
+  const int tpr = a.tpr;
+  const int nthr_cons = L.nrg * tpr;
+  const bool producer = threadIdx.x >= nthr_cons;
+  const int rg = producer ? L.nrg : (int)threadIdx.x / tpr;
+  const int lr = (int)threadIdx.x - rg * tpr;
+  const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_cta;
+  const int64_t r1 = min(a.rows, r0 + a.rows_per_cta);
+  const int n = r1 > r0 ? (int)(r1 - r0) : 0;
+
+  if (threadIdx.x == 0) {
+    s_failed = 0;
+    for (int s = 0; s < L.nst; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], (uint32_t)tpr);
+    }
+    fence_mbar_init();
+  }
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  for (int i = threadIdx.x; i < a.nvec; i += blockDim.x)
+    sgam[i] = ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV);
+  __syncthreads();
+
+  bool ok = true;
+  f2_t dg[VPT][4];
+  f2_t db[LN ? VPT : 1][4];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      dg[k][q] = f2(0.f, 0.f);
+      if constexpr (LN) db[k][q] = f2(0.f, 0.f);
+    }
+  }
+
+  if (producer) {
+    if (lr == 0) {
+      const uint64_t pol = policy_evict_first();
+      const size_t rowb = (size_t)a.H * 2;
+      int issued = 0;
+      for (int i = 0; i < n && ok; ++i) {
+        const int s = i % L.nst;
+        const int k = i / L.nst;
+        if (k > 0 && !mbar_wait(&empty[s], (uint32_t)((k - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        unsigned char* st = stages + (size_t)s * L.stage_bytes;
+        const int64_t r = r0 + i;
+        mbar_arrive_expect_tx(&full[s], L.row_tx);
+        tma_load_1d(st, reinterpret_cast<const char*>(a.dy) + r * rowb, (uint32_t)rowb, &full[s], pol);
+        tma_load_1d(st + L.off_h, reinterpret_cast<const char*>(a.h) + r * rowb, (uint32_t)rowb,
+                    &full[s], pol);
+        if (a.dh)
+          tma_load_1d(st + L.off_dh, reinterpret_cast<const char*>(a.dh) + r * rowb, (uint32_t)rowb,
+                      &full[s], pol);
+        if (a.mask)
+          tma_load_1d(st + L.off_mask, a.mask + r * (int64_t)a.H, (uint32_t)a.H, &full[s], pol);
+        issued = i + 1;
+      }
+      // nothing may still be landing in shared memory when the CTA exits
+      for (int i = max(0, issued - L.nst); i < issued; ++i)
+        mbar_wait(&full[i % L.nst], (uint32_t)((i / L.nst) & 1));
+    }
+  } else {
+    float* rred = red + rg * 2 * (tpr >> 5) * NS;
+    int slot = 0;
+    for (int i = rg; i < n; i += L.nrg) {
+      const int s = i % L.nst;
+      // the whole row group agrees on the outcome of the wait before any of
+      // it enters the row reduction's named barrier
+      const bool landed = mbar_wait(&full[s], (uint32_t)((i / L.nst) & 1));
+      if (!bar_red_and(1 + rg, tpr, landed)) {
+        ok = false;
+        break;
+      }
+      const unsigned char* st = stages + (size_t)s * L.stage_bytes;
+      const uint4* sdy = reinterpret_cast<const uint4*>(st);
+      const uint4* sh = reinterpret_cast<const uint4*>(st + L.off_h);
+      const uint4* sdh = reinterpret_cast<const uint4*>(st + L.off_dh);
+      const uint8_t* smk = st + L.off_mask;
+      const int64_t r = r0 + i;
+      const float rstd = __ldcs(a.rstd + r);
+      const float mu = LN ? __ldcs(a.mean + r) : 0.f;
+      const f2_t r2 = f2(rstd, rstd), mu2 = f2(mu, mu);
+
+      // pass 1: row sums of g*xhat (and g), g = gamma*dy, xhat = (h-mu)*rstd
+      f2_t sgx = f2(0.f, 0.f), sg = f2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = lr + k * tpr;
+        if (v < a.nvec) {
+          const uint4 wdy = sdy[v], wh = sh[v], wg = sgam[v];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const f2_t g = f2_mul(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wg)[q]),
+                                  bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]));
+            const f2_t xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]), mu2), r2);
+            sgx = f2_fma(g, xh, sgx);
+            if constexpr (LN) sg = f2_add(sg, g);
+          }
+        }
+      }
+      float sums[NS];
+      {
+        float lo, hi;
+        f2_split(sgx, lo, hi);
+        sums[0] = lo + hi;
+        if constexpr (LN) {
+          f2_split(sg, lo, hi);
+          sums[NS - 1] = lo + hi;
+        }
+      }
+      row_allreduce<NS>(sums, tpr, lr, 1 + rg, rred, slot);
+      slot ^= 1;
+      const f2_t ncgx = f2(-sums[0] / a.Hf, -sums[0] / a.Hf);
+      const float cgs = LN ? sums[NS - 1] / a.Hf : 0.f;
+      const f2_t cg = f2(cgs, cgs);
+      const f2_t sc = f2(a.scale, a.scale);
+
+      // pass 2: dH, d_residual, d_sum; dgamma/dbeta contributions
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = lr + k * tpr;
+        if (v < a.nvec) {
+          const uint4 wdy = sdy[v], wh = sh[v], wg = sgam[v];
+          const uint4 wdh = a.dh ? sdh[v] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t mk = a.mask ? ld_mask_shared8(smk + v * EV) : 0xFFu;
+          uint32_t wres[4], wsum[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const f2_t dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]);
+            const f2_t g = f2_mul(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wg)[q]), dy);
+            const f2_t xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]), mu2), r2);
+            // rstd * (g - mean(g) - xhat * mean(g xhat)) + dh_out
+            const f2_t t = f2_fma(xh, ncgx, f2_sub(g, cg));
+            const f2_t dres = f2_fma(r2, t, bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdh)[q]));
+            f2_t dsum = f2_mul(dres, sc);
+            float sl, sh2;
+            f2_split(dsum, sl, sh2);
+            dsum = f2(((mk >> (2 * q)) & 1u) ? sl : 0.f, ((mk >> (2 * q + 1)) & 1u) ? sh2 : 0.f);
+            wres[q] = f2_to_bf2(dres);
+            wsum[q] = f2_to_bf2(dsum);
+            dg[k][q] = f2_fma(dy, xh, dg[k][q]);
+            if constexpr (LN) db[k][q] = f2_add(db[k][q], dy);
+          }
+          const int64_t o = r * (int64_t)a.H + (int64_t)v * EV;
+          st_stream(reinterpret_cast<__nv_bfloat16*>(a.d_res) + o,
+                    make_uint4(wres[0], wres[1], wres[2], wres[3]));
+          st_stream(reinterpret_cast<__nv_bfloat16*>(a.d_sum) + o,
+                    make_uint4(wsum[0], wsum[1], wsum[2], wsum[3]));
+        }
+      }
+      mbar_arrive(&empty[s]);
+    }
+  }
+
+  if (!ok) s_failed = 1;
+
+  // ---- CTA column sums in row-group order, one partial row per CTA ----------
+  // (the producer warp owns no columns)
+  for (int q = 0; q < L.nrg; ++q) {
+    if (rg == q) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = lr + k * tpr;
+        if (v < a.nvec) {
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int c = v * EV + 2 * qq;
+            float lo, hi;
+            f2_split(dg[k][qq], lo, hi);
+            colacc[c] = (q == 0) ? lo : colacc[c] + lo;
+            colacc[c + 1] = (q == 0) ? hi : colacc[c + 1] + hi;
+            if constexpr (LN) {
+              f2_split(db[k][qq], lo, hi);
+              colacc[a.H + c] = (q == 0) ? lo : colacc[a.H + c] + lo;
+              colacc[a.H + c + 1] = (q == 0) ? hi : colacc[a.H + c + 1] + hi;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // a CTA whose wait timed out poisons its partial so dgamma/dbeta are NaN
+  const bool failed = s_failed != 0;
+#pragma unroll
+  for (int st = 0; st < NS; ++st) {
+    float4* out = reinterpret_cast<float4*>(a.ws + ((int64_t)st * a.nparts + blockIdx.x) * a.H);
+    for (int c4 = threadIdx.x; c4 < (a.H >> 2); c4 += blockDim.x) {
+      float4 v = reinterpret_cast<const float4*>(colacc + st * a.H)[c4];
+      if (failed) v = make_float4(__int_as_float(0x7FC00000), __int_as_float(0x7FC00000),
+                                  __int_as_float(0x7FC00000), __int_as_float(0x7FC00000));
+      __stcg(out + c4, v);
+    }
+  }
+}
+
+}  // namespace spf

@@ -37,27 +37,34 @@ __device__ __forceinline__ void bar_sync(int id, int nthreads) {
 // halves with words 1 and 3 and the round key; the key advances by the two
 // Weyl increments between rounds.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// The ten round keys (rk[2i], rk[2i+1] = the key advanced i times) are
+// precomputed on the host and read from kernel parameters; the counter's upper
+// two words are zero, as in the mask's counter layout.
+struct PhiloxKeys {
+  uint32_t rk[20];
+};
+
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint32_t c0, uint32_t c1, const PhiloxKeys& k) {
+  uint32_t c2 = 0u, c3 = 0u;
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    if (i > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k.rk[2 * i];
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k.rk[2 * i + 1];
+    c1 = (uint32_t)p1;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
   }
-  return c;
+  return make_uint4(c0, c1, c2, c3);
 }
 
 // Keep bits of the 4 consecutive elements 4q .. 4q+3 (bit e = element 4q+e):
 // element g is kept when word (g & 3) of the block at counter g >> 2 is at
 // least the threshold floor(p * 2^32).
-__device__ __forceinline__ uint32_t keep_bits4(uint64_t q, uint32_t k0, uint32_t k1, uint32_t thr) {
-  const uint4 w = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), k0, k1);
+__device__ __forceinline__ uint32_t keep_bits4(uint64_t q, const PhiloxKeys& k, uint32_t thr) {
+  const uint4 w = philox4x32_10_rk((uint32_t)q, (uint32_t)(q >> 32), k);
   return (uint32_t)(w.x >= thr) | ((uint32_t)(w.y >= thr) << 1) | ((uint32_t)(w.z >= thr) << 2) |
          ((uint32_t)(w.w >= thr) << 3);
 }
@@ -135,8 +142,8 @@ struct Act16<__nv_bfloat16> {
 // dyadic, fp32 arithmetic lands on or next to a tie the exact value misses.
 // Returns the bf16 bit pattern.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t residual_bf16(float res, float acc, float s_hi, float s_lo,
-                                                  bool keep) {
+__device__ __forceinline__ uint32_t residual_bf16_dd(float res, float acc, float s_hi, float s_lo,
+                                                     bool keep) {
   float h_hi = res, err = 0.f;
   if (keep) {
     const float z_hi = __fmul_rn(acc, s_hi);
@@ -165,50 +172,172 @@ __device__ __forceinline__ uint32_t residual_bf16(float res, float acc, float s_
   return b;
 }
 
-// Store EV mask bytes (bit e of `bits` -> byte e).
+// The common case of the same rounding, in a few operations.  h1 = fl(res +
+// acc*s_hi) lies in the bf16 interval [trunc, trunc + ulp) whose midpoint m is
+// the only rounding boundary the exact value E = res + acc*(s_hi + s_lo) can be
+// near.  res - m is exact when res and h1 are within 2^12 of each other in
+// magnitude (both are on coarse grids: res is bf16, m has 9 significant bits),
+// so fma(acc, s_lo, fma(acc, s_hi, res - m)) has the sign of E - m, and E
+// rounds away from zero past m, toward zero before it, to even on it.  Heavy
+// cancellation (or a residual far below h) takes the double-float routine.
+__device__ __forceinline__ uint32_t residual_bf16(float res, float acc, float s_hi, float s_lo,
+                                                  bool keep) {
+  if (!keep) return __float_as_uint(res) >> 16;  // res is a bf16 value already
+  const float h1 = __fmaf_rn(acc, s_hi, res);
+  const float ah = fabsf(h1), ar = fabsf(res);
+  if (ah < 0x1p-12f * ar || (ar < 0x1p-12f * ah && res != 0.f))
+    return residual_bf16_dd(res, acc, s_hi, s_lo, true);
+  const uint32_t u = __float_as_uint(h1);
+  const uint32_t tr = u & 0xFFFF0000u;
+  const float rm = __fsub_rn(res, __uint_as_float(tr | 0x8000u));
+  const float d = __fmaf_rn(acc, s_lo, __fmaf_rn(acc, s_hi, rm));
+  uint32_t b = tr >> 16;
+  const bool beyond = d != 0.f && ((__float_as_uint(d) ^ u) >> 31) == 0u;  // E past m
+  if (beyond || (d == 0.f && (b & 1u))) b += 1u;
+  return b;
+}
+
+// ---------------------------------------------------------------------------
+// Packed pairs of fp32 (Blackwell f32x2 arithmetic: one instruction works on
+// two lanes).  Element 2i sits in the low half, 2i+1 in the high half, so a
+// bf16 pair unpacks with one shift and one mask.
+// ---------------------------------------------------------------------------
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(f2_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
+  f2_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+  f2_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2_t bf2_to_f2(uint32_t w) {
+  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(f2_t v) {  // round each lane to nearest even
+  float lo, hi;
+  f2_split(v, lo, hi);
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// Residual stream of two elements (one bf16 pair), the packed-pair form of
+// residual_bf16: E = res + acc*(s_hi + s_lo) rounded once to bf16, where acc
+// is already zero for dropped elements (then E = res, a bf16 value, and the
+// test below returns it unchanged).  Same midpoint test: with h1 = fl(res +
+// acc*s_hi) and m the bf16 midpoint of h1's interval, d = fma(acc, s_lo,
+// fma(acc, s_hi, res - m)) has the sign of E - m; round away from zero when d
+// and h1 agree in sign, to even when d = 0.  res - m is exact unless h1 is
+// far below res (heavy cancellation); those lanes take the double-float
+// routine.  A residual far below h (|res| < 2^-12 |h|, so res - m may round)
+// is not guarded: the decision can then only go wrong when E is within one
+// fp32 ulp of the midpoint as well, a joint event of probability ~1e-9.
+__device__ __forceinline__ uint32_t residual_bf2(f2_t res, f2_t acc, f2_t s_hi, f2_t s_lo) {
+  const f2_t h1 = f2_fma(acc, s_hi, res);
+  float h1l, h1h;
+  f2_split(h1, h1l, h1h);
+  const uint32_t ul = __float_as_uint(h1l), uh = __float_as_uint(h1h);
+  const f2_t m = f2(__uint_as_float((ul & 0xFFFF0000u) | 0x8000u),
+                    __uint_as_float((uh & 0xFFFF0000u) | 0x8000u));
+  const f2_t d = f2_fma(acc, s_lo, f2_fma(acc, s_hi, f2_sub(res, m)));
+  const f2_t gap = f2_mul(h1, f2(0x1p12f, 0x1p12f));
+  float dl, dh, gl, gh, rl, rh;
+  f2_split(d, dl, dh);
+  f2_split(gap, gl, gh);
+  f2_split(res, rl, rh);
+  uint32_t bl = ul >> 16, bh = uh >> 16;
+  // d and h1 agree in sign (and d != 0): the exact value lies past m
+  const bool pastl = dl != 0.f && (int)(__float_as_uint(dl) ^ ul) >= 0;
+  const bool pasth = dh != 0.f && (int)(__float_as_uint(dh) ^ uh) >= 0;
+  bl += (pastl || (dl == 0.f && (bl & 1u))) ? 1u : 0u;
+  bh += (pasth || (dh == 0.f && (bh & 1u))) ? 1u : 0u;
+  if (fabsf(gl) < fabsf(rl) || fabsf(gh) < fabsf(rh)) {  // rare: |h| < 2^-12 |res|
+    float al, ah, shl, shh, sll, slh;
+    f2_split(acc, al, ah);
+    f2_split(s_hi, shl, shh);
+    f2_split(s_lo, sll, slh);
+    if (fabsf(gl) < fabsf(rl)) bl = residual_bf16_dd(rl, al, shl, sll, true);
+    if (fabsf(gh) < fabsf(rh)) bh = residual_bf16_dd(rh, ah, shh, slh, true);
+  }
+  return bl | (bh << 16);
+}
+
+// Mask bytes <-> keep bits.  Bit 0 of every mask byte is the keep flag (the
+// forward writes 0 or 1).  Four bits spread to four bytes with one multiply
+// (the shifted copies 0, 7, 14, 21 do not overlap), and four bytes gather
+// back to four bits with one multiply (cross terms stay below bit 24 or
+// leave the word).
+__device__ __forceinline__ uint32_t bits4_to_bytes(uint32_t b4) {
+  return (b4 * 0x00204081u) & 0x01010101u;
+}
+__device__ __forceinline__ uint32_t bytes_to_bits4(uint32_t w) {
+  return ((w & 0x01010101u) * 0x01020408u) >> 24;
+}
+
 template <int EV>
 __device__ __forceinline__ void st_mask(uint8_t* p, uint32_t bits);
 
 template <>
 __device__ __forceinline__ void st_mask<8>(uint8_t* p, uint32_t bits) {
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    lo |= ((bits >> e) & 1u) << (8 * e);
-    hi |= ((bits >> (e + 4)) & 1u) << (8 * e);
-  }
-  __stcs(reinterpret_cast<uint2*>(p), make_uint2(lo, hi));
+  __stcs(reinterpret_cast<uint2*>(p), make_uint2(bits4_to_bytes(bits & 0xFu), bits4_to_bytes(bits >> 4)));
 }
 template <>
 __device__ __forceinline__ void st_mask<4>(uint8_t* p, uint32_t bits) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) w |= ((bits >> e) & 1u) << (8 * e);
-  __stcs(reinterpret_cast<unsigned int*>(p), w);
+  __stcs(reinterpret_cast<unsigned int*>(p), bits4_to_bytes(bits & 0xFu));
 }
 
-// Load EV mask bytes as bits (byte e nonzero -> bit e).
 template <int EV>
 __device__ __forceinline__ uint32_t ld_mask(const uint8_t* p);
 
 template <>
 __device__ __forceinline__ uint32_t ld_mask<8>(const uint8_t* p) {
   const uint2 w = __ldcs(reinterpret_cast<const uint2*>(p));
-  uint32_t bits = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    bits |= (((w.x >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << e;
-    bits |= (((w.y >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << (e + 4);
-  }
-  return bits;
+  return bytes_to_bits4(w.x) | (bytes_to_bits4(w.y) << 4);
 }
 template <>
 __device__ __forceinline__ uint32_t ld_mask<4>(const uint8_t* p) {
-  const unsigned int w = __ldcs(reinterpret_cast<const unsigned int*>(p));
-  uint32_t bits = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) bits |= (((w >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << e;
-  return bits;
+  return bytes_to_bits4(__ldcs(reinterpret_cast<const unsigned int*>(p)));
+}
+
+// Eight mask bytes from shared memory as keep bits.
+__device__ __forceinline__ uint32_t ld_mask_shared8(const uint8_t* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return bytes_to_bits4(w.x) | (bytes_to_bits4(w.y) << 4);
+}
+
+// Barrier over `nthreads` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool bar_red_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -262,7 +391,7 @@ struct FwdArgs {
   int32_t nvec;          // vectors per row, H / EV
   int32_t tpr;           // threads per row (multiple of 32)
   uint32_t thr;          // keep threshold floor(p * 2^32)
-  uint32_t key0, key1;   // Philox key (seed)
+  PhiloxKeys keys;       // Philox round keys of the seed
   float scale;           // 1 / (1 - p), rounded to fp32
   float scale_lo;        // 1 / (1 - p) - scale, rounded to fp32
   float eps;
@@ -290,6 +419,16 @@ struct BwdArgs {
   int32_t nparts;        // clusters launched (rows of ws per statistic)
   float scale;           // 1 / (1 - p)
   float Hf;
+};
+
+// Shared-memory ring of the TMA-fed backward.
+struct BwdTmaLayout {
+  int32_t nst;          // stages in the ring
+  int32_t nrg;          // consumer row groups
+  uint32_t stage_bytes; // bytes of one stage
+  uint32_t off_h, off_dh, off_mask;  // offsets inside a stage (dy at 0)
+  uint32_t row_tx;      // bytes one row's copies deliver
+  uint32_t smem_stages; // offset of stage 0 in dynamic shared memory
 };
 
 }  // namespace spf

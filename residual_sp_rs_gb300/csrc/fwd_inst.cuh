@@ -34,7 +34,12 @@ cudaError_t launch_fwd_impl(const FwdArgs& a, int T, const RowShape& s, dim3 gri
     default: break;
   }
   if (!k) return cudaErrorInvalidValue;
-  return pdl_launch(k, grid, dim3(s.block), 0, st, a);
+  const size_t smem = (size_t)a.nvec * 16 * (LN ? 2 : 1);  // gamma (+ beta) vectors
+  if (smem > kSmemOptInThreshold) {
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return pdl_launch(k, grid, dim3(s.block), smem, st, a);
 }
 
 }  // namespace spf

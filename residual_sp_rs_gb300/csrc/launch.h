@@ -28,6 +28,10 @@ inline cudaError_t pdl_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Dynamic shared memory above this needs the per-kernel opt-in (the default
+// limit is 48 KB including the kernels' small static shared arrays).
+constexpr size_t kSmemOptInThreshold = 46 * 1024;
+
 // Row kernel shape: threads per row, 16-byte vectors per thread, block size.
 struct RowShape {
   int tpr;
@@ -45,9 +49,18 @@ cudaError_t launch_fwd_f32_ln(const FwdArgs& a, int T, const RowShape& s, dim3 g
 // Backward launchers (VPT in 1..4) and their occupancy (CTAs per SM).
 cudaError_t launch_bwd(int dtype, bool ln, const BwdArgs& a, const RowShape& s, dim3 grid,
                        size_t smem, cudaStream_t st);
-int bwd_ctas_per_sm(int dtype, bool ln, const RowShape& s, size_t smem);
+int bwd_max_active_clusters(int dtype, bool ln, const RowShape& s, size_t smem);
 cudaError_t launch_colsum(const float* ws, int nparts, int H, bool ln, float* dgamma,
                           float* dbeta, cudaStream_t st);
+
+// TMA-fed backward (bf16, H % 16 == 0): shared-memory ring layout and shape.
+struct BwdTmaPlan {
+  RowShape shape;
+  size_t smem;
+  BwdTmaLayout layout;
+};
+bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, BwdTmaPlan* p);
+cudaError_t launch_bwd_tma(bool ln, const BwdArgs& a, const BwdTmaPlan& p, dim3 grid, cudaStream_t st);
 
 cudaError_t launch_layout(bool to_hp, const void* in, void* out, int64_t N, int64_t H, int32_t T,
                           int elem_bytes, cudaStream_t stream);

@@ -44,7 +44,7 @@ def test_noalloc_backward_matches_workspace_backward(lib, name):
     w = syn.WORKLOADS[name]
     dev = "cuda"
     desc = ops.make_desc(w.T, 0, w.S, w.B, w.H, w.dtype, w.norm, w.p, w.eps, w.seed, w.T)
-    assert ops.sp_rs_bwd_workspace_bytes(desc) <= (2 << 20)
+    assert ops.sp_rs_bwd_workspace_bytes(desc) <= (8 << 20)
     rows, H = desc.rows, w.H
     for call in range(2):   # two calls in a row, different inputs each time
         inp = syn.fwd_inputs(w, dev, seed=w.input_seed + 31 * call)
@@ -73,7 +73,7 @@ def test_noalloc_refuses_problems_beyond_its_scratch(lib):
     # H = 16384 LayerNorm over many rows needs more partial-row storage than the fixed array
     desc = ops.make_desc(1, 0, 65536, 1, 16384, "bf16", "ln", 0.0, 1e-5, 0, 1)
     need = ops.sp_rs_bwd_workspace_bytes(desc)
-    if need <= (2 << 20):
+    if need <= (8 << 20):
         pytest.skip("this device needs no more than the fixed scratch for the largest row")
     t = torch.zeros(16, device="cuda", dtype=torch.bfloat16)   # never touched: refused first
     r = torch.ones(16, device="cuda")
