@@ -25,7 +25,7 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
   if (H % 16 != 0) return false;  // mask rows must be whole 16-byte copies
   const int nvec = (int)(H / 8);
   int tpr = 32;
-  while (tpr < 512 && (nvec + tpr - 1) / tpr > 4) tpr *= 2;
+  while (tpr < 256 && (nvec + tpr - 1) / tpr > 4) tpr *= 2;
   const int vpt = (nvec + tpr - 1) / tpr;
   if (vpt > 4) return false;
   const int nrg = tpr >= 256 ? 1 : 256 / tpr;

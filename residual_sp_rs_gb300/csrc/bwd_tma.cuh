@@ -23,7 +23,7 @@
 namespace spf {
 
 template <bool LN, int VPT>
-__global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
+__global__ void __launch_bounds__(288, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
   using V = Act16<__nv_bfloat16>;
   constexpr int EV = 8;
   constexpr int NS = LN ? 2 : 1;
