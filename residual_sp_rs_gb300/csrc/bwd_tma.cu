@@ -18,47 +18,51 @@ void (*tma_kernel(int vpt))(const BwdArgs, const BwdTmaLayout) {
 }
 
 constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, rounded up
+constexpr int kBwdTmaConsumers = 512;  // consumer threads per CTA
 
 }  // namespace
 
 bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, BwdTmaPlan* p) {
   if (H % 16 != 0) return false;  // mask rows must be whole 16-byte copies
   const int nvec = (int)(H / 8);
+  // 16 consumer warps; a row group of tpr threads holds <= 4 vectors per
+  // thread (<= 2 for LayerNorm, whose dbeta accumulators double the registers)
+  const int vcap = ln ? 2 : 4;
   int tpr = 32;
-  while (tpr < 256 && (nvec + tpr - 1) / tpr > 4) tpr *= 2;
+  while (tpr < kBwdTmaConsumers && (nvec + tpr - 1) / tpr > vcap) tpr *= 2;
   const int vpt = (nvec + tpr - 1) / tpr;
   if (vpt > 4) return false;
-  const int nrg = tpr >= 256 ? 1 : 256 / tpr;
+  int nrg = kBwdTmaConsumers / tpr;  // rows per stage, one per row group
   const uint32_t rowb = (uint32_t)H * 2;
-  BwdTmaLayout L = {};
-  L.off_h = rowb;
-  L.off_dh = 2 * rowb;
-  L.off_mask = has_dh ? 3 * rowb : 2 * rowb;
-  L.stage_bytes = L.off_mask + (has_mask ? (uint32_t)H : 0u);
-  L.stage_bytes = (L.stage_bytes + 15u) & ~15u;
-  L.row_tx = 2 * rowb + (has_dh ? rowb : 0u) + (has_mask ? (uint32_t)H : 0u);
-  L.nrg = nrg;
   const size_t fixed_base = (size_t)(ln ? 2 : 1) * H * 4 + (size_t)nvec * 16;
   const size_t budget = (size_t)max_smem - kStaticSmem;
-  int nst = 0;
-  // stages, rounded down to a multiple of the row groups (each owns its stages)
-  for (int cand = 64; cand >= 2 * nrg; --cand) {
-    if (cand % nrg) continue;
-    const size_t bars = 16 * (((size_t)2 * cand * 8 + 15) / 16);
-    if (bars + fixed_base + (size_t)cand * L.stage_bytes <= budget) {
-      nst = cand;
-      break;
+  for (; nrg >= 1; nrg /= 2) {
+    BwdTmaLayout L = {};
+    const uint32_t blk = (uint32_t)nrg * rowb;  // one tensor's rows in a stage
+    L.off_h = blk;
+    L.off_dh = 2 * blk;
+    L.off_mask = has_dh ? 3 * blk : 2 * blk;
+    L.stage_bytes = (L.off_mask + (has_mask ? (uint32_t)(nrg * H) : 0u) + 15u) & ~15u;
+    L.nrg = nrg;
+    int nst = 0;
+    for (int cand = 8; cand >= 2; --cand) {
+      const size_t bars = 16 * (((size_t)2 * cand * 8 + 15) / 16);
+      if (bars + fixed_base + (size_t)cand * L.stage_bytes <= budget) {
+        nst = cand;
+        break;
+      }
     }
+    if (nst < 2) continue;  // fewer rows per stage, and try again
+    L.nst = nst;
+    L.smem_stages = (uint32_t)(16 * (((size_t)2 * nst * 8 + 15) / 16) + fixed_base);
+    p->layout = L;
+    p->shape.tpr = tpr;
+    p->shape.vpt = vpt;
+    p->shape.block = nrg * tpr + 32;
+    p->smem = L.smem_stages + (size_t)nst * L.stage_bytes;
+    return true;
   }
-  if (nst < 2 * nrg) return false;
-  L.nst = nst;
-  L.smem_stages = (uint32_t)(16 * (((size_t)2 * nst * 8 + 15) / 16) + fixed_base);
-  p->layout = L;
-  p->shape.tpr = tpr;
-  p->shape.vpt = vpt;
-  p->shape.block = nrg * tpr + 32;
-  p->smem = L.smem_stages + (size_t)nst * L.stage_bytes;
-  return true;
+  return false;
 }
 
 cudaError_t launch_bwd_tma(bool ln, const BwdArgs& a, const BwdTmaPlan& p, dim3 grid,

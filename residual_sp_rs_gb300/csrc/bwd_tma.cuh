@@ -2,11 +2,12 @@
 // memory by the Tensor Memory Accelerator (bulk copies + mbarriers).
 //
 // One persistent CTA per SM owns a contiguous block of token rows.  A
-// producer warp keeps a ring of NST one-row stages full: for each row it
-// issues one bulk copy per input tensor (dy, h, dh_out, mask) on the stage's
-// "full" mbarrier.  Consumer row groups (tpr threads each) take rows
-// round-robin, compute from shared memory and release the stage on its
-// "empty" mbarrier.  The loads of up to NST rows are in flight at all times,
+// producer warp keeps a ring of NST stages full; a stage holds nrg
+// consecutive rows, one per consumer row group, and is filled with one bulk
+// copy per input tensor (dy, h, dh_out, mask) on the stage's "full" mbarrier.
+// Each row group (tpr threads) computes its row of the stage from shared
+// memory; the stage is released on its "empty" mbarrier when all consumers
+// are done.  The loads of up to NST*nrg rows are in flight at all times,
 // without holding them in registers, so the HBM pipe stays busy through the
 // row reductions and the stores.  dgamma/dbeta accumulate in registers per
 // thread-owned column; at the end the CTA adds its row groups in order and
@@ -23,7 +24,7 @@
 namespace spf {
 
 template <bool LN, int VPT>
-__global__ void __launch_bounds__(288, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
+__global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
   using V = Act16<__nv_bfloat16>;
   constexpr int EV = 8;
   constexpr int NS = LN ? 2 : 1;
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(288, 1) sp_bwd_tma_kernel(const BwdArgs a, con
     s_failed = 0;
     for (int s = 0; s < L.nst; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], (uint32_t)tpr);
+      mbar_init(&empty[s], (uint32_t)(L.nrg * tpr));  // every consumer releases
     }
     fence_mbar_init();
   }
@@ -71,52 +72,59 @@ __global__ void __launch_bounds__(288, 1) sp_bwd_tma_kernel(const BwdArgs a, con
     }
   }
 
+  const int nstage = (n + L.nrg - 1) / L.nrg;  // stages this CTA fills
   if (producer) {
     if (lr == 0) {
       const uint64_t pol = policy_evict_first();
       const size_t rowb = (size_t)a.H * 2;
       int issued = 0;
-      for (int i = 0; i < n && ok; ++i) {
-        const int s = i % L.nst;
-        const int k = i / L.nst;
+      for (int j = 0; j < nstage && ok; ++j) {
+        const int s = j % L.nst;
+        const int k = j / L.nst;
         if (k > 0 && !mbar_wait(&empty[s], (uint32_t)((k - 1) & 1))) {
           ok = false;
           break;
         }
         unsigned char* st = stages + (size_t)s * L.stage_bytes;
-        const int64_t r = r0 + i;
-        mbar_arrive_expect_tx(&full[s], L.row_tx);
-        tma_load_1d(st, reinterpret_cast<const char*>(a.dy) + r * rowb, (uint32_t)rowb, &full[s], pol);
-        tma_load_1d(st + L.off_h, reinterpret_cast<const char*>(a.h) + r * rowb, (uint32_t)rowb,
-                    &full[s], pol);
+        const int64_t r = r0 + (int64_t)j * L.nrg;
+        const int rows = min(L.nrg, n - j * L.nrg);
+        const uint32_t bb = (uint32_t)(rows * rowb);  // bytes of one bf16 tensor's rows
+        mbar_arrive_expect_tx(&full[s], bb * (a.dh ? 3u : 2u) + (a.mask ? (uint32_t)(rows * a.H) : 0u));
+        tma_load_1d(st, reinterpret_cast<const char*>(a.dy) + r * rowb, bb, &full[s], pol);
+        tma_load_1d(st + L.off_h, reinterpret_cast<const char*>(a.h) + r * rowb, bb, &full[s], pol);
         if (a.dh)
-          tma_load_1d(st + L.off_dh, reinterpret_cast<const char*>(a.dh) + r * rowb, (uint32_t)rowb,
-                      &full[s], pol);
+          tma_load_1d(st + L.off_dh, reinterpret_cast<const char*>(a.dh) + r * rowb, bb, &full[s], pol);
         if (a.mask)
-          tma_load_1d(st + L.off_mask, a.mask + r * (int64_t)a.H, (uint32_t)a.H, &full[s], pol);
-        issued = i + 1;
+          tma_load_1d(st + L.off_mask, a.mask + r * (int64_t)a.H, (uint32_t)(rows * a.H), &full[s], pol);
+        issued = j + 1;
       }
       // nothing may still be landing in shared memory when the CTA exits
-      for (int i = max(0, issued - L.nst); i < issued; ++i)
-        mbar_wait(&full[i % L.nst], (uint32_t)((i / L.nst) & 1));
+      for (int j = max(0, issued - L.nst); j < issued; ++j)
+        mbar_wait(&full[j % L.nst], (uint32_t)((j / L.nst) & 1));
     }
   } else {
     float* rred = red + rg * 2 * (tpr >> 5) * NS;
     int slot = 0;
-    for (int i = rg; i < n; i += L.nrg) {
-      const int s = i % L.nst;
+    for (int j = 0; j < nstage; ++j) {
+      const int s = j % L.nst;
       // the whole row group agrees on the outcome of the wait before any of
       // it enters the row reduction's named barrier
-      const bool landed = mbar_wait(&full[s], (uint32_t)((i / L.nst) & 1));
+      const bool landed = mbar_wait(&full[s], (uint32_t)((j / L.nst) & 1));
       if (!bar_red_and(1 + rg, tpr, landed)) {
         ok = false;
         break;
       }
+      const int i = j * L.nrg + rg;  // this row group's row of the stage
+      if (i >= n) {                  // last stage short of rows: just release it
+        mbar_arrive(&empty[s]);
+        continue;
+      }
       const unsigned char* st = stages + (size_t)s * L.stage_bytes;
-      const uint4* sdy = reinterpret_cast<const uint4*>(st);
-      const uint4* sh = reinterpret_cast<const uint4*>(st + L.off_h);
-      const uint4* sdh = reinterpret_cast<const uint4*>(st + L.off_dh);
-      const uint8_t* smk = st + L.off_mask;
+      const size_t rofs = (size_t)rg * a.H * 2;  // this row inside each tensor's block
+      const uint4* sdy = reinterpret_cast<const uint4*>(st + rofs);
+      const uint4* sh = reinterpret_cast<const uint4*>(st + L.off_h + rofs);
+      const uint4* sdh = reinterpret_cast<const uint4*>(st + L.off_dh + rofs);
+      const uint8_t* smk = st + L.off_mask + (size_t)rg * a.H;
       const int64_t r = r0 + i;
       const float rstd = __ldcs(a.rstd + r);
       const float mu = LN ? __ldcs(a.mean + r) : 0.f;

@@ -427,7 +427,6 @@ struct BwdTmaLayout {
   int32_t nrg;          // consumer row groups
   uint32_t stage_bytes; // bytes of one stage
   uint32_t off_h, off_dh, off_mask;  // offsets inside a stage (dy at 0)
-  uint32_t row_tx;      // bytes one row's copies deliver
   uint32_t smem_stages; // offset of stage 0 in dynamic shared memory
 };
 
