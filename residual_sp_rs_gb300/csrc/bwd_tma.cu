@@ -53,6 +53,8 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
       }
     }
     if (nst < 2) continue;  // fewer rows per stage, and try again
+    // row groups wider than a warp synchronise on named barriers 1..nrg
+    if (tpr > 32 && nrg > 15) return false;
     L.nst = nst;
     L.smem_stages = (uint32_t)(16 * (((size_t)2 * nst * 8 + 15) / 16) + fixed_base);
     p->layout = L;

@@ -109,8 +109,11 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
       const int s = j % L.nst;
       // the whole row group agrees on the outcome of the wait before any of
       // it enters the row reduction's named barrier
+      // (one-warp row groups vote; wider ones use their named barrier, id <= 8)
       const bool landed = mbar_wait(&full[s], (uint32_t)((j / L.nst) & 1));
-      if (!bar_red_and(1 + rg, tpr, landed)) {
+      const bool all_landed =
+          tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
+      if (!all_landed) {
         ok = false;
         break;
       }
