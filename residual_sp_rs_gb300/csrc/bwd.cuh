@@ -185,12 +185,15 @@ __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
   cl.sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 
-// Second pass: dgamma[c] (and dbeta[c]) = sum over partial rows p = 0..nparts-1
-// in that order.  blockDim (32, 8): x picks a float4 column group, y a stride
-// class of partial rows; the 8 stride sums are added in y order.
-__global__ void __launch_bounds__(256) sp_colsum_kernel(const float* ws, int nparts, int H,
-                                                        float* dgamma, float* dbeta) {
-  __shared__ float4 part[8][32];
+// Second pass: dgamma[c] (and dbeta[c]) = the sum over partial rows
+// p = 0..nparts-1.  blockDim (32, 32): x picks a float4 column of a 32-column
+// group, y a stride class of partial rows (p = y, y+32, ...).  Each thread
+// issues all its loads (up to 8 per round) before adding, then warp 0 adds the
+// 32 stride sums in y order.  The order is fixed, so the result is
+// bit-identical from run to run.
+__global__ void __launch_bounds__(1024) sp_colsum_kernel(const float* ws, int nparts, int H,
+                                                         float* dgamma, float* dbeta) {
+  __shared__ float4 part[32][32];
   grid_dep_wait();
   grid_dep_launch_dependents();
   const int stat = blockIdx.y;
@@ -200,20 +203,28 @@ __global__ void __launch_bounds__(256) sp_colsum_kernel(const float* ws, int npa
   const int n4 = H / 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (c4 < n4) {
-    for (int p = threadIdx.y; p < nparts; p += 8) {
-      const float4 w = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)p * H) + c4);
-      acc.x += w.x;
-      acc.y += w.y;
-      acc.z += w.z;
-      acc.w += w.w;
+    for (int p0 = threadIdx.y; p0 < nparts; p0 += 32 * 8) {
+      float4 w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int p = p0 + 32 * u;
+        w[u] = p < nparts ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)p * H) + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += w[u].x;
+        acc.y += w[u].y;
+        acc.z += w[u].z;
+        acc.w += w[u].w;
+      }
     }
   }
   part[threadIdx.y][threadIdx.x] = acc;
   __syncthreads();
   if (threadIdx.y == 0 && c4 < n4) {
     float4 s = part[0][threadIdx.x];
-#pragma unroll
-    for (int q = 1; q < 8; ++q) {
+    for (int q = 1; q < 32; ++q) {
       const float4 w = part[q][threadIdx.x];
       s.x += w.x;
       s.y += w.y;

@@ -34,7 +34,7 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
   if (vpt > 4) return false;
   int nrg = kBwdTmaConsumers / tpr;  // rows per stage, one per row group
   const uint32_t rowb = (uint32_t)H * 2;
-  const size_t fixed_base = (size_t)(ln ? 2 : 1) * H * 4 + (size_t)nvec * 16;
+  const size_t fixed_base = (size_t)nvec * 16;  // gamma vectors
   const size_t budget = (size_t)max_smem - kStaticSmem;
   for (; nrg >= 1; nrg /= 2) {
     BwdTmaLayout L = {};
@@ -53,6 +53,8 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
       }
     }
     if (nst < 2) continue;  // fewer rows per stage, and try again
+    // at the end the ring holds the row groups' column sums
+    if ((size_t)nst * L.stage_bytes < (size_t)nrg * (ln ? 2 : 1) * H * 4) continue;
     // row groups wider than a warp synchronise on named barriers 1..nrg
     if (tpr > 32 && nrg > 15) return false;
     L.nst = nst;

@@ -10,8 +10,9 @@
 // are done.  The loads of up to NST*nrg rows are in flight at all times,
 // without holding them in registers, so the HBM pipe stays busy through the
 // row reductions and the stores.  dgamma/dbeta accumulate in registers per
-// thread-owned column; at the end the CTA adds its row groups in order and
-// writes one fp32 partial row, which sp_colsum_kernel reduces in CTA order.
+// thread-owned column; at the end the row groups' sums go to the idle ring,
+// are added in row-group order and written as one fp32 partial row per CTA,
+// which sp_colsum_kernel reduces in CTA order.
 //
 // If a wait times out (a copy that never lands), the CTA stops, waits (with a
 // limit) for what it issued, and poisons its dgamma/dbeta partial with NaN so
@@ -33,8 +34,7 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   extern __shared__ __align__(16) unsigned char dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
   uint64_t* empty = full + L.nst;
-  float* colacc = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // [NS][H]
-  uint4* sgam = reinterpret_cast<uint4*>(colacc + NS * a.H);                          // [nvec]
+  uint4* sgam = reinterpret_cast<uint4*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // [nvec]
   unsigned char* stages = dsm + L.smem_stages;
 
   const int tpr = a.tpr;
@@ -46,18 +46,41 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   const int64_t r1 = min(a.rows, r0 + a.rows_per_cta);
   const int n = r1 > r0 ? (int)(r1 - r0) : 0;
 
-  if (threadIdx.x == 0) {
+  const int nstage = (n + L.nrg - 1) / L.nrg;  // stages this CTA fills
+  const size_t rowb = (size_t)a.H * 2;
+  const uint64_t pol = policy_evict_first();
+  // Producer: fill stage j (rows j*nrg ..) once the ring slot is free.
+  auto issue_stage = [&](int j) {
+    const int s = j % L.nst;
+    unsigned char* st = stages + (size_t)s * L.stage_bytes;
+    const int64_t r = r0 + (int64_t)j * L.nrg;
+    const int rows = min(L.nrg, n - j * L.nrg);
+    const uint32_t bb = (uint32_t)(rows * rowb);  // bytes of one bf16 tensor's rows
+    mbar_arrive_expect_tx(&full[s], bb * (a.dh ? 3u : 2u) + (a.mask ? (uint32_t)(rows * a.H) : 0u));
+    tma_load_1d(st, reinterpret_cast<const char*>(a.dy) + r * rowb, bb, &full[s], pol);
+    tma_load_1d(st + L.off_h, reinterpret_cast<const char*>(a.h) + r * rowb, bb, &full[s], pol);
+    if (a.dh)
+      tma_load_1d(st + L.off_dh, reinterpret_cast<const char*>(a.dh) + r * rowb, bb, &full[s], pol);
+    if (a.mask)
+      tma_load_1d(st + L.off_mask, a.mask + r * (int64_t)a.H, (uint32_t)(rows * a.H), &full[s], pol);
+  };
+  const bool lead = producer && lr == 0;
+  int issued = 0;
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  if (lead) {
     s_failed = 0;
     for (int s = 0; s < L.nst; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], (uint32_t)(L.nrg * tpr));  // every consumer releases
     }
     fence_mbar_init();
+    // the first ring's worth of rows goes out before anything else happens
+    for (; issued < min(nstage, L.nst); ++issued) issue_stage(issued);
+  } else if (!producer) {
+    for (int i = threadIdx.x; i < a.nvec; i += nthr_cons)
+      sgam[i] = ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV);
   }
-  grid_dep_wait();
-  grid_dep_launch_dependents();
-  for (int i = threadIdx.x; i < a.nvec; i += blockDim.x)
-    sgam[i] = ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV);
   __syncthreads();
 
   bool ok = true;
@@ -72,30 +95,15 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
     }
   }
 
-  const int nstage = (n + L.nrg - 1) / L.nrg;  // stages this CTA fills
   if (producer) {
-    if (lr == 0) {
-      const uint64_t pol = policy_evict_first();
-      const size_t rowb = (size_t)a.H * 2;
-      int issued = 0;
-      for (int j = 0; j < nstage && ok; ++j) {
-        const int s = j % L.nst;
-        const int k = j / L.nst;
-        if (k > 0 && !mbar_wait(&empty[s], (uint32_t)((k - 1) & 1))) {
+    if (lead) {
+      for (int j = issued; j < nstage; ++j) {
+        const int k = j / L.nst;  // >= 1: the slot was used k times before
+        if (!mbar_wait(&empty[j % L.nst], (uint32_t)((k - 1) & 1))) {
           ok = false;
           break;
         }
-        unsigned char* st = stages + (size_t)s * L.stage_bytes;
-        const int64_t r = r0 + (int64_t)j * L.nrg;
-        const int rows = min(L.nrg, n - j * L.nrg);
-        const uint32_t bb = (uint32_t)(rows * rowb);  // bytes of one bf16 tensor's rows
-        mbar_arrive_expect_tx(&full[s], bb * (a.dh ? 3u : 2u) + (a.mask ? (uint32_t)(rows * a.H) : 0u));
-        tma_load_1d(st, reinterpret_cast<const char*>(a.dy) + r * rowb, bb, &full[s], pol);
-        tma_load_1d(st + L.off_h, reinterpret_cast<const char*>(a.h) + r * rowb, bb, &full[s], pol);
-        if (a.dh)
-          tma_load_1d(st + L.off_dh, reinterpret_cast<const char*>(a.dh) + r * rowb, bb, &full[s], pol);
-        if (a.mask)
-          tma_load_1d(st + L.off_mask, a.mask + r * (int64_t)a.H, (uint32_t)(rows * a.H), &full[s], pol);
+        issue_stage(j);
         issued = j + 1;
       }
       // nothing may still be landing in shared memory when the CTA exits
@@ -205,44 +213,40 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   }
 
   if (!ok) s_failed = 1;
+  __syncthreads();  // every stage consumed and landed: the ring is free
 
-  // ---- CTA column sums in row-group order, one partial row per CTA ----------
-  // (the producer warp owns no columns)
-  for (int q = 0; q < L.nrg; ++q) {
-    if (rg == q) {
+  // ---- dgamma/dbeta: row groups' column sums into the ring, added in order ---
+  float* part = reinterpret_cast<float*>(stages);  // [nrg][NS][H]
+  if (!producer) {
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int v = lr + k * tpr;
-        if (v < a.nvec) {
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lr + k * tpr;
+      if (v < a.nvec) {
+        float* dst = part + (size_t)rg * NS * a.H + v * EV;
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const int c = v * EV + 2 * qq;
-            float lo, hi;
-            f2_split(dg[k][qq], lo, hi);
-            colacc[c] = (q == 0) ? lo : colacc[c] + lo;
-            colacc[c + 1] = (q == 0) ? hi : colacc[c + 1] + hi;
-            if constexpr (LN) {
-              f2_split(db[k][qq], lo, hi);
-              colacc[a.H + c] = (q == 0) ? lo : colacc[a.H + c] + lo;
-              colacc[a.H + c + 1] = (q == 0) ? hi : colacc[a.H + c + 1] + hi;
-            }
+        for (int q = 0; q < 4; ++q) {
+          float lo, hi;
+          f2_split(dg[k][q], lo, hi);
+          dst[2 * q] = lo;
+          dst[2 * q + 1] = hi;
+          if constexpr (LN) {
+            f2_split(db[k][q], lo, hi);
+            dst[a.H + 2 * q] = lo;
+            dst[a.H + 2 * q + 1] = hi;
           }
         }
       }
     }
-    __syncthreads();
   }
+  __syncthreads();
   // a CTA whose wait timed out poisons its partial so dgamma/dbeta are NaN
   const bool failed = s_failed != 0;
-#pragma unroll
-  for (int st = 0; st < NS; ++st) {
-    float4* out = reinterpret_cast<float4*>(a.ws + ((int64_t)st * a.nparts + blockIdx.x) * a.H);
-    for (int c4 = threadIdx.x; c4 < (a.H >> 2); c4 += blockDim.x) {
-      float4 v = reinterpret_cast<const float4*>(colacc + st * a.H)[c4];
-      if (failed) v = make_float4(__int_as_float(0x7FC00000), __int_as_float(0x7FC00000),
-                                  __int_as_float(0x7FC00000), __int_as_float(0x7FC00000));
-      __stcg(out + c4, v);
-    }
+  for (int c = threadIdx.x; c < NS * a.H; c += blockDim.x) {
+    float acc = part[c];
+    for (int g = 1; g < L.nrg; ++g) acc += part[(size_t)g * NS * a.H + c];
+    const int st = c / a.H;
+    __stcg(a.ws + ((int64_t)st * a.nparts + blockIdx.x) * a.H + (c - st * a.H),
+           failed ? __int_as_float(0x7FC00000) : acc);
   }
 }
 
