@@ -197,12 +197,26 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   a.Hf = (float)pr.H;
   a.dropout = desc->p > 0.0f ? 1 : 0;
 
+  if (inject_launch_failure()) return SP_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (pr.dtype == SP_BF16) {
+    int dev = 0, sms = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return SP_ERR_CUDA;
+    FwdTmaPlan tp;
+    if (plan_fwd_tma(pr.H, pr.T, ln, optin, pr.rows, sms, &tp)) {
+      a.tpr = tp.shape.tpr;
+      const dim3 grid((unsigned)((pr.rows + tp.layout.rows_per_cta - 1) / tp.layout.rows_per_cta));
+      return from_cuda(ln ? launch_fwd_tma_ln(a, pr.T, tp, grid, cs)
+                          : launch_fwd_tma_rms(a, pr.T, tp, grid, cs));
+    }
+  }
   const RowShape s = row_shape(pr.nvec, fwd_vpt_cap(pr.T));
   a.tpr = s.tpr;
   const int rpc = s.block / s.tpr;
   const dim3 grid((unsigned)((pr.rows + rpc - 1) / rpc));
-  if (inject_launch_failure()) return SP_ERR_CUDA;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pr.dtype == SP_BF16)
     e = ln ? launch_fwd_bf16_ln(a, pr.T, s, grid, cs) : launch_fwd_bf16_rms(a, pr.T, s, grid, cs);

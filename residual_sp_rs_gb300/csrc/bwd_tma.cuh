@@ -113,6 +113,12 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   } else {
     float* rred = red + rg * 2 * (tpr >> 5) * NS;
     int slot = 0;
+    // row statistics one row ahead, so their DRAM latency hides behind a row
+    float rstd_n = 0.f, mu_n = 0.f;
+    if (rg < n) {
+      rstd_n = __ldcs(a.rstd + r0 + rg);
+      if constexpr (LN) mu_n = __ldcs(a.mean + r0 + rg);
+    }
     for (int j = 0; j < nstage; ++j) {
       const int s = j % L.nst;
       // the whole row group agrees on the outcome of the wait before any of
@@ -137,8 +143,12 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
       const uint4* sdh = reinterpret_cast<const uint4*>(st + L.off_dh + rofs);
       const uint8_t* smk = st + L.off_mask + (size_t)rg * a.H;
       const int64_t r = r0 + i;
-      const float rstd = __ldcs(a.rstd + r);
-      const float mu = LN ? __ldcs(a.mean + r) : 0.f;
+      const float rstd = rstd_n;
+      const float mu = mu_n;
+      if (i + L.nrg < n) {
+        rstd_n = __ldcs(a.rstd + r + L.nrg);
+        if constexpr (LN) mu_n = __ldcs(a.mean + r + L.nrg);
+      }
       const f2_t r2 = f2(rstd, rstd), mu2 = f2(mu, mu);
 
       // pass 1: row sums of g*xhat (and g), g = gamma*dy, xhat = (h-mu)*rstd

@@ -421,6 +421,16 @@ struct BwdArgs {
   float Hf;
 };
 
+// Shared-memory ring of the TMA-fed forward.
+struct FwdTmaLayout {
+  int32_t nst;           // stages in the ring
+  int32_t nrg;           // consumer row groups (rows per stage)
+  uint32_t stage_bytes;  // bytes of one stage
+  uint32_t blk;          // bytes of one tensor's rows in a stage (nrg * H * 2)
+  uint32_t smem_stages;  // offset of stage 0 in dynamic shared memory
+  int64_t rows_per_cta;
+};
+
 // Shared-memory ring of the TMA-fed backward.
 struct BwdTmaLayout {
   int32_t nst;          // stages in the ring

@@ -1,0 +1,264 @@
+// fwd_tma.cuh -- forward of the SP region with rows streamed through shared
+// memory by the Tensor Memory Accelerator (bf16).
+//
+// One persistent CTA per SM owns a contiguous block of token rows.  A
+// producer warp keeps a ring of NST stages full; a stage holds nrg
+// consecutive rows (one per consumer row group) of each of the T partials
+// and of the residual, each filled with one bulk copy on the stage's "full"
+// mbarrier.  Consumer row groups reduce, mask, add and normalise their row
+// from shared memory and release the stage on its "empty" mbarrier, so the
+// arithmetic of one stage overlaps the loads of the next ones.  gamma/beta
+// are kept in shared memory as fp32.  Used when a stage of rows fits twice in
+// shared memory; longer rows (T*H large) take the register-resident kernel.
+//
+// If a wait times out, the row group stops and writes NaN into the rstd of
+// the rows it did not finish, so the failure is visible in the outputs.
+#pragma once
+
+#include "common.cuh"
+#include "tma.cuh"
+
+namespace spf {
+
+// bf16 residual stream for a pair when p > 0: as residual_bf2, without the
+// tie-to-even branch.  With 1/(1-p) irrational in binary (s_lo != 0) the exact
+// value E = res + acc*s never equals a bf16 midpoint unless acc = 0, and then
+// E = res is a bf16 value whose midpoint test (d < 0) needs no tie rule.
+__device__ __forceinline__ uint32_t residual_bf2_drop(f2_t res, f2_t acc, f2_t s_hi, f2_t s_lo) {
+  const f2_t h1 = f2_fma(acc, s_hi, res);
+  float h1l, h1h;
+  f2_split(h1, h1l, h1h);
+  const uint32_t ul = __float_as_uint(h1l), uh = __float_as_uint(h1h);
+  const f2_t m = f2(__uint_as_float((ul & 0xFFFF0000u) | 0x8000u),
+                    __uint_as_float((uh & 0xFFFF0000u) | 0x8000u));
+  const f2_t d = f2_fma(acc, s_lo, f2_fma(acc, s_hi, f2_sub(res, m)));
+  const f2_t gap = f2_mul(h1, f2(0x1p12f, 0x1p12f));
+  float dl, dh, gl, gh, rl, rh;
+  f2_split(d, dl, dh);
+  f2_split(gap, gl, gh);
+  f2_split(res, rl, rh);
+  // past the midpoint, away from zero: d and h1 agree in sign, d != 0
+  const uint32_t pl = (int)(__float_as_uint(dl) ^ (ul & 0x80000000u)) > 0 ? 0x1u : 0u;
+  const uint32_t ph = (int)(__float_as_uint(dh) ^ (uh & 0x80000000u)) > 0 ? 0x10000u : 0u;
+  uint32_t w = __byte_perm(ul, uh, 0x7632) + pl + ph;
+  if (fabsf(gl) < fabsf(rl) || fabsf(gh) < fabsf(rh)) {  // rare: |h| < 2^-12 |res|
+    float al, ah, shl, shh, sll, slh;
+    f2_split(acc, al, ah);
+    f2_split(s_hi, shl, shh);
+    f2_split(s_lo, sll, slh);
+    uint32_t bl = w & 0xFFFFu, bh = w >> 16;
+    if (fabsf(gl) < fabsf(rl)) bl = residual_bf16_dd(rl, al, shl, sll, true);
+    if (fabsf(gh) < fabsf(rh)) bh = residual_bf16_dd(rh, ah, shh, slh, true);
+    w = bl | (bh << 16);
+  }
+  return w;
+}
+
+template <int T, bool LN, int VPT>
+__global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, const FwdTmaLayout L) {
+  constexpr int EV = 8;
+  __shared__ float red[2 * 32 * 2];
+  extern __shared__ __align__(16) unsigned char dsm[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
+  uint64_t* empty = full + L.nst;
+  float* sgb = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // gamma[H], beta[H]
+  unsigned char* stages = dsm + L.smem_stages;
+
+  const int tpr = a.tpr;
+  const int nthr_cons = L.nrg * tpr;
+  const bool producer = threadIdx.x >= nthr_cons;
+  const int rg = producer ? L.nrg : (int)threadIdx.x / tpr;
+  const int lr = (int)threadIdx.x - rg * tpr;
+  const int64_t r0 = (int64_t)blockIdx.x * L.rows_per_cta;
+  const int64_t r1 = min(a.rows, r0 + L.rows_per_cta);
+  const int n = r1 > r0 ? (int)(r1 - r0) : 0;
+  const int nstage = (n + L.nrg - 1) / L.nrg;
+  const size_t rowb = (size_t)a.H * 2;
+  const uint64_t pol = policy_evict_first();
+
+  auto issue_stage = [&](int j) {
+    const int s = j % L.nst;
+    unsigned char* st = stages + (size_t)s * L.stage_bytes;
+    const int64_t r = r0 + (int64_t)j * L.nrg;  // local row of the stage's first row
+    const int rows = min(L.nrg, n - j * L.nrg);
+    const uint32_t bb = (uint32_t)(rows * rowb);
+    mbar_arrive_expect_tx(&full[s], bb * (uint32_t)(T + 1));
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+      tma_load_1d(st + (size_t)t * L.blk, reinterpret_cast<const char*>(a.P[t]) + (a.grow0 + r) * rowb,
+                  bb, &full[s], pol);
+    tma_load_1d(st + (size_t)T * L.blk, reinterpret_cast<const char*>(a.residual) + r * rowb, bb,
+                &full[s], pol);
+  };
+
+  const bool lead = producer && lr == 0;
+  int issued = 0;
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  if (lead) {
+    for (int s = 0; s < L.nst; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], (uint32_t)nthr_cons);
+    }
+    fence_mbar_init();
+    for (; issued < min(nstage, L.nst); ++issued) issue_stage(issued);
+  } else if (!producer) {
+    for (int i = threadIdx.x; i < a.nvec; i += nthr_cons) {
+      float g[EV];
+      Act16<__nv_bfloat16>::unpack(ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV), g);
+#pragma unroll
+      for (int e = 0; e < EV; ++e) sgb[i * EV + e] = g[e];
+      if constexpr (LN) {
+        Act16<__nv_bfloat16>::unpack(ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.beta) + i * EV), g);
+#pragma unroll
+        for (int e = 0; e < EV; ++e) sgb[a.H + i * EV + e] = g[e];
+      }
+    }
+  }
+  __syncthreads();
+
+  if (producer) {
+    if (lead) {
+      for (int j = issued; j < nstage; ++j) {
+        const int k = j / L.nst;
+        if (!mbar_wait(&empty[j % L.nst], (uint32_t)((k - 1) & 1))) break;
+        issue_stage(j);
+        issued = j + 1;
+      }
+      for (int j = max(0, issued - L.nst); j < issued; ++j)
+        mbar_wait(&full[j % L.nst], (uint32_t)((j / L.nst) & 1));
+    }
+    return;
+  }
+
+  float* rred = red + rg * 2 * (tpr >> 5);
+  const f2_t shi = f2(a.scale, a.scale), slo = f2(a.scale_lo, a.scale_lo);
+  for (int j = 0; j < nstage; ++j) {
+    const int s = j % L.nst;
+    const bool landed = mbar_wait(&full[s], (uint32_t)((j / L.nst) & 1));
+    const bool all_landed =
+        tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
+    if (!all_landed) {  // give up: mark this row group's remaining rows
+      for (int i = j * L.nrg + rg; i < n; i += L.nrg)
+        if (lr == 0) a.rstd[r0 + i] = __int_as_float(0x7FC00000);
+      return;
+    }
+    const int i = j * L.nrg + rg;
+    if (i >= n) {
+      mbar_arrive(&empty[s]);
+      continue;
+    }
+    const unsigned char* st = stages + (size_t)s * L.stage_bytes + (size_t)rg * rowb;
+    const int64_t r = r0 + i;
+    const int64_t grow = a.grow0 + r;
+
+    // ---- reduce, mask, dropout, residual add; store h and the mask --------
+    f2_t hf[VPT][4];
+    f2_t s2 = f2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lr + k * tpr;
+      if (v < a.nvec) {
+        uint4 pw[T];
+#pragma unroll
+        for (int t = 0; t < T; ++t) pw[t] = reinterpret_cast<const uint4*>(st + (size_t)t * L.blk)[v];
+        const uint4 rw = reinterpret_cast<const uint4*>(st + (size_t)T * L.blk)[v];
+        const uint64_t g0 = (uint64_t)(grow * a.H + (int64_t)v * EV);
+        uint32_t keep = 0xFFu;
+        if (a.dropout)
+          keep = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
+        uint32_t hw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          f2_t acc = bf2_to_f2(reinterpret_cast<const uint32_t*>(&pw[0])[q]);
+#pragma unroll
+          for (int t = 1; t < T; ++t)
+            acc = f2_add(acc, bf2_to_f2(reinterpret_cast<const uint32_t*>(&pw[t])[q]));
+          const f2_t res = bf2_to_f2(reinterpret_cast<const uint32_t*>(&rw)[q]);
+          if (a.dropout) {
+            float al, ah;
+            f2_split(acc, al, ah);
+            acc = f2(((keep >> (2 * q)) & 1u) ? al : 0.f, ((keep >> (2 * q + 1)) & 1u) ? ah : 0.f);
+            hw[q] = residual_bf2_drop(res, acc, shi, slo);
+          } else {
+            hw[q] = residual_bf2(res, acc, shi, slo);
+          }
+          hf[k][q] = bf2_to_f2(hw[q]);
+          s2 = LN ? f2_add(s2, hf[k][q]) : f2_fma(hf[k][q], hf[k][q], s2);
+        }
+        const int64_t o = r * (int64_t)a.H + (int64_t)v * EV;
+        st_stream(reinterpret_cast<__nv_bfloat16*>(a.h) + o, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+        if (a.mask) st_mask<EV>(a.mask + o, keep);
+      }
+    }
+    mbar_arrive(&empty[s]);  // the stage is no longer read
+
+    // ---- row statistics -----------------------------------------------------
+    float sv[1];
+    {
+      float lo, hi;
+      f2_split(s2, lo, hi);
+      sv[0] = lo + hi;
+    }
+    row_allreduce<1>(sv, tpr, lr, 1 + rg, rred, 0);
+    float mu = 0.f, rstd;
+    if constexpr (LN) {
+      mu = sv[0] / a.Hf;
+      const f2_t mu2 = f2(mu, mu);
+      f2_t q2 = f2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (lr + k * tpr < a.nvec) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const f2_t dd = f2_sub(hf[k][q], mu2);
+            q2 = f2_fma(dd, dd, q2);
+          }
+        }
+      }
+      float qv[1];
+      {
+        float lo, hi;
+        f2_split(q2, lo, hi);
+        qv[0] = lo + hi;
+      }
+      row_allreduce<1>(qv, tpr, lr, 1 + rg, rred, 1);
+      rstd = 1.0f / sqrtf(qv[0] / a.Hf + a.eps);
+    } else {
+      rstd = 1.0f / sqrtf(sv[0] / a.Hf + a.eps);
+    }
+
+    // ---- y = gamma * xhat (+ beta), one rounding ------------------------------
+    const f2_t r2 = f2(rstd, rstd), mu2 = f2(mu, mu);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lr + k * tpr;
+      if (v < a.nvec) {
+        const float4* gp = reinterpret_cast<const float4*>(sgb + v * EV);
+        uint32_t yw[4];
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const float4 g4 = gp[q2];
+          const f2_t ga = f2(g4.x, g4.y), gb = f2(g4.z, g4.w);
+          if constexpr (LN) {
+            const float4 b4 = reinterpret_cast<const float4*>(sgb + a.H + v * EV)[q2];
+            yw[2 * q2] = f2_to_bf2(f2_fma(ga, f2_mul(f2_sub(hf[k][2 * q2], mu2), r2), f2(b4.x, b4.y)));
+            yw[2 * q2 + 1] =
+                f2_to_bf2(f2_fma(gb, f2_mul(f2_sub(hf[k][2 * q2 + 1], mu2), r2), f2(b4.z, b4.w)));
+          } else {
+            yw[2 * q2] = f2_to_bf2(f2_mul(ga, f2_mul(hf[k][2 * q2], r2)));
+            yw[2 * q2 + 1] = f2_to_bf2(f2_mul(gb, f2_mul(hf[k][2 * q2 + 1], r2)));
+          }
+        }
+        st_stream(reinterpret_cast<__nv_bfloat16*>(a.y) + r * (int64_t)a.H + (int64_t)v * EV,
+                  make_uint4(yw[0], yw[1], yw[2], yw[3]));
+      }
+    }
+    if (lr == 0) {
+      a.rstd[r] = rstd;
+      if constexpr (LN) a.mean[r] = mu;
+    }
+  }
+}
+
+}  // namespace spf

@@ -1,0 +1,42 @@
+// fwd_tma_inst.cuh -- instances of the TMA-fed forward for one norm over
+// T = 1..8 and VPT = 1..4.
+#pragma once
+
+#include "fwd_tma.cuh"
+#include "launch.h"
+
+namespace spf {
+
+template <bool LN, int T>
+inline void (*fwd_tma_kernel_for_vpt(int vpt))(const FwdArgs, const FwdTmaLayout) {
+  switch (vpt) {
+    case 1: return sp_fwd_tma_kernel<T, LN, 1>;
+    case 2: return sp_fwd_tma_kernel<T, LN, 2>;
+    case 3: return sp_fwd_tma_kernel<T, LN, 3>;
+    case 4: return sp_fwd_tma_kernel<T, LN, 4>;
+    default: return nullptr;
+  }
+}
+
+template <bool LN>
+cudaError_t launch_fwd_tma_impl(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid,
+                                cudaStream_t st) {
+  void (*k)(const FwdArgs, const FwdTmaLayout) = nullptr;
+  switch (T) {
+    case 1: k = fwd_tma_kernel_for_vpt<LN, 1>(p.shape.vpt); break;
+    case 2: k = fwd_tma_kernel_for_vpt<LN, 2>(p.shape.vpt); break;
+    case 3: k = fwd_tma_kernel_for_vpt<LN, 3>(p.shape.vpt); break;
+    case 4: k = fwd_tma_kernel_for_vpt<LN, 4>(p.shape.vpt); break;
+    case 5: k = fwd_tma_kernel_for_vpt<LN, 5>(p.shape.vpt); break;
+    case 6: k = fwd_tma_kernel_for_vpt<LN, 6>(p.shape.vpt); break;
+    case 7: k = fwd_tma_kernel_for_vpt<LN, 7>(p.shape.vpt); break;
+    case 8: k = fwd_tma_kernel_for_vpt<LN, 8>(p.shape.vpt); break;
+    default: break;
+  }
+  if (!k) return cudaErrorInvalidValue;
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  if (e != cudaSuccess) return e;
+  return pdl_launch(k, grid, dim3(p.shape.block), p.smem, st, a, p.layout);
+}
+
+}  // namespace spf

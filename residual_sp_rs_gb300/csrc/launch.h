@@ -62,6 +62,16 @@ struct BwdTmaPlan {
 bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, BwdTmaPlan* p);
 cudaError_t launch_bwd_tma(bool ln, const BwdArgs& a, const BwdTmaPlan& p, dim3 grid, cudaStream_t st);
 
+// TMA-fed forward (bf16, rows short enough for a two-stage ring).
+struct FwdTmaPlan {
+  RowShape shape;
+  size_t smem;
+  FwdTmaLayout layout;
+};
+bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms, FwdTmaPlan* p);
+cudaError_t launch_fwd_tma_rms(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_tma_ln(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid, cudaStream_t st);
+
 cudaError_t launch_layout(bool to_hp, const void* in, void* out, int64_t N, int64_t H, int32_t T,
                           int elem_bytes, cudaStream_t stream);
 
