@@ -196,6 +196,7 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   a.eps = desc->eps;
   a.Hf = (float)pr.H;
   a.dropout = desc->p > 0.0f ? 1 : 0;
+  a.dyadic_scale = a.scale_lo == 0.0f ? 1 : 0;
 
   if (inject_launch_failure()) return SP_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -397,6 +397,7 @@ struct FwdArgs {
   float eps;
   float Hf;              // H as float
   int32_t dropout;       // p > 0
+  int32_t dyadic_scale;  // 1/(1-p) is exact in fp32 (scale_lo == 0): bf16 ties can occur
 };
 
 struct BwdArgs {

@@ -20,10 +20,11 @@
 
 namespace spf {
 
-// bf16 residual stream for a pair when p > 0: as residual_bf2, without the
-// tie-to-even branch.  With 1/(1-p) irrational in binary (s_lo != 0) the exact
-// value E = res + acc*s never equals a bf16 midpoint unless acc = 0, and then
-// E = res is a bf16 value whose midpoint test (d < 0) needs no tie rule.
+// bf16 residual stream for a pair when 1/(1-p) is not a dyadic fraction
+// (s_lo != 0): as residual_bf2, without the tie-to-even branch.  Then the
+// exact value E = res + acc*s is not a bf16 midpoint unless acc = 0, and for
+// acc = 0, E = res is a bf16 value whose midpoint test (d < 0) needs no tie
+// rule.  (p = 0.5, 0.75, ... make s dyadic; those take residual_bf2.)
 __device__ __forceinline__ uint32_t residual_bf2_drop(f2_t res, f2_t acc, f2_t s_hi, f2_t s_lo) {
   const f2_t h1 = f2_fma(acc, s_hi, res);
   float h1l, h1h;
@@ -179,10 +180,9 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
             float al, ah;
             f2_split(acc, al, ah);
             acc = f2(((keep >> (2 * q)) & 1u) ? al : 0.f, ((keep >> (2 * q + 1)) & 1u) ? ah : 0.f);
-            hw[q] = residual_bf2_drop(res, acc, shi, slo);
-          } else {
-            hw[q] = residual_bf2(res, acc, shi, slo);
           }
+          hw[q] = (a.dropout && !a.dyadic_scale) ? residual_bf2_drop(res, acc, shi, slo)
+                                                 : residual_bf2(res, acc, shi, slo);
           hf[k][q] = bf2_to_f2(hw[q]);
           s2 = LN ? f2_add(s2, hf[k][q]) : f2_fma(hf[k][q], hf[k][q], s2);
         }
