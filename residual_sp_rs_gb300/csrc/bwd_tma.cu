@@ -6,15 +6,22 @@ namespace spf {
 
 namespace {
 
-template <bool LN>
-void (*tma_kernel(int vpt))(const BwdArgs, const BwdTmaLayout) {
+template <bool LN, bool DH, bool MASK>
+void (*tma_kernel_v(int vpt))(const BwdArgs, const BwdTmaLayout) {
   switch (vpt) {
-    case 1: return sp_bwd_tma_kernel<LN, 1>;
-    case 2: return sp_bwd_tma_kernel<LN, 2>;
-    case 3: return sp_bwd_tma_kernel<LN, 3>;
-    case 4: return sp_bwd_tma_kernel<LN, 4>;
+    case 1: return sp_bwd_tma_kernel<LN, 1, DH, MASK>;
+    case 2: return sp_bwd_tma_kernel<LN, 2, DH, MASK>;
+    case 3:
+      if constexpr (!LN) return sp_bwd_tma_kernel<LN, 3, DH, MASK>;  // LayerNorm stays <= 2
+      return nullptr;
     default: return nullptr;
   }
+}
+
+template <bool LN>
+void (*tma_kernel(int vpt, bool dh, bool mask))(const BwdArgs, const BwdTmaLayout) {
+  if (dh) return mask ? tma_kernel_v<LN, true, true>(vpt) : tma_kernel_v<LN, true, false>(vpt);
+  return mask ? tma_kernel_v<LN, false, true>(vpt) : tma_kernel_v<LN, false, false>(vpt);
 }
 
 constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, rounded up
@@ -25,16 +32,16 @@ constexpr int kBwdTmaConsumers = 512;  // consumer threads per CTA
 bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, BwdTmaPlan* p) {
   if (H % 16 != 0) return false;  // mask rows must be whole 16-byte copies
   const int nvec = (int)(H / 8);
-  // 16 consumer warps; a row group of tpr threads holds <= 4 vectors per
-  // thread (<= 2 for LayerNorm, whose dbeta accumulators double the registers)
-  const int vcap = ln ? 2 : 4;
+  // 16 consumer warps; a row group of tpr threads holds <= 3 vectors per
+  // thread (<= 2 for LayerNorm, whose dbeta accumulators add registers)
+  const int vcap = ln ? 2 : 3;
   int tpr = 32;
   while (tpr < kBwdTmaConsumers && (nvec + tpr - 1) / tpr > vcap) tpr *= 2;
   const int vpt = (nvec + tpr - 1) / tpr;
-  if (vpt > 4) return false;
+  if (vpt > vcap) return false;
   int nrg = kBwdTmaConsumers / tpr;  // rows per stage, one per row group
   const uint32_t rowb = (uint32_t)H * 2;
-  const size_t fixed_base = (size_t)nvec * 16;  // gamma vectors
+  const size_t fixed_base = (size_t)H * 4;  // gamma, fp32
   const size_t budget = (size_t)max_smem - kStaticSmem;
   for (; nrg >= 1; nrg /= 2) {
     BwdTmaLayout L = {};
@@ -71,8 +78,9 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
 
 cudaError_t launch_bwd_tma(bool ln, const BwdArgs& a, const BwdTmaPlan& p, dim3 grid,
                            cudaStream_t st) {
-  void (*k)(const BwdArgs, const BwdTmaLayout) = ln ? tma_kernel<true>(p.shape.vpt)
-                                                    : tma_kernel<false>(p.shape.vpt);
+  const bool dh = a.dh != nullptr, mask = a.mask != nullptr;
+  void (*k)(const BwdArgs, const BwdTmaLayout) = ln ? tma_kernel<true>(p.shape.vpt, dh, mask)
+                                                    : tma_kernel<false>(p.shape.vpt, dh, mask);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;

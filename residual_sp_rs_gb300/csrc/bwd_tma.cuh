@@ -6,13 +6,15 @@
 // consecutive rows, one per consumer row group, and is filled with one bulk
 // copy per input tensor (dy, h, dh_out, mask) on the stage's "full" mbarrier.
 // Each row group (tpr threads) computes its row of the stage from shared
-// memory; the stage is released on its "empty" mbarrier when all consumers
-// are done.  The loads of up to NST*nrg rows are in flight at all times,
-// without holding them in registers, so the HBM pipe stays busy through the
-// row reductions and the stores.  dgamma/dbeta accumulate in registers per
-// thread-owned column; at the end the row groups' sums go to the idle ring,
-// are added in row-group order and written as one fp32 partial row per CTA,
-// which sp_colsum_kernel reduces in CTA order.
+// memory; the stage is released on its "empty" mbarrier as soon as every
+// consumer has read it.  The loads of up to NST*nrg rows are in flight at all
+// times, without holding them in registers, so the HBM pipe stays busy
+// through the row reductions and the stores.  dy and xhat stay in registers
+// between the two passes over a row; gamma sits in shared memory as fp32.
+// dgamma/dbeta accumulate in registers per thread-owned column; at the end
+// the row groups' sums go to the idle ring, are added in row-group order and
+// written as one fp32 partial row per CTA, which sp_colsum_kernel reduces in
+// CTA order.
 //
 // If a wait times out (a copy that never lands), the CTA stops, waits (with a
 // limit) for what it issued, and poisons its dgamma/dbeta partial with NaN so
@@ -24,9 +26,8 @@
 
 namespace spf {
 
-template <bool LN, int VPT>
-__global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
-  using V = Act16<__nv_bfloat16>;
+template <bool LN, int VPT, bool DH, bool MASK>
+__global__ void __maxnreg__(120) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
   constexpr int EV = 8;
   constexpr int NS = LN ? 2 : 1;
   __shared__ float red[2 * 32 * 2];
@@ -34,35 +35,37 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   extern __shared__ __align__(16) unsigned char dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
   uint64_t* empty = full + L.nst;
-  uint4* sgam = reinterpret_cast<uint4*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // [nvec]
+  float* sgam = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // gamma [H] fp32
   unsigned char* stages = dsm + L.smem_stages;
 
-  const int tpr = a.tpr;
-  const int nthr_cons = L.nrg * tpr;
+  // kernel parameters used in the hot loop, held in registers
+  const int H = a.H, nvec = a.nvec, tpr = a.tpr, nrg = L.nrg, nst = L.nst;
+  const float invH = 1.0f / a.Hf;
+  const float scale = a.scale;
+  const int nthr_cons = nrg * tpr;
   const bool producer = threadIdx.x >= nthr_cons;
-  const int rg = producer ? L.nrg : (int)threadIdx.x / tpr;
+  const int rg = producer ? nrg : (int)threadIdx.x / tpr;
   const int lr = (int)threadIdx.x - rg * tpr;
   const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_cta;
   const int64_t r1 = min(a.rows, r0 + a.rows_per_cta);
   const int n = r1 > r0 ? (int)(r1 - r0) : 0;
+  const int nstage = (n + nrg - 1) / nrg;  // stages this CTA fills
+  const size_t rowb = (size_t)H * 2;
 
-  const int nstage = (n + L.nrg - 1) / L.nrg;  // stages this CTA fills
-  const size_t rowb = (size_t)a.H * 2;
-  const uint64_t pol = policy_evict_first();
-  // Producer: fill stage j (rows j*nrg ..) once the ring slot is free.
-  auto issue_stage = [&](int j) {
-    const int s = j % L.nst;
+  // Producer: fill stage j (rows j*nrg ..) of the ring.
+  auto issue_stage = [&](int j, uint64_t pol) {
+    const int s = j % nst;
     unsigned char* st = stages + (size_t)s * L.stage_bytes;
-    const int64_t r = r0 + (int64_t)j * L.nrg;
-    const int rows = min(L.nrg, n - j * L.nrg);
+    const int64_t r = r0 + (int64_t)j * nrg;
+    const int rows = min(nrg, n - j * nrg);
     const uint32_t bb = (uint32_t)(rows * rowb);  // bytes of one bf16 tensor's rows
-    mbar_arrive_expect_tx(&full[s], bb * (a.dh ? 3u : 2u) + (a.mask ? (uint32_t)(rows * a.H) : 0u));
+    mbar_arrive_expect_tx(&full[s], bb * (DH ? 3u : 2u) + (MASK ? (uint32_t)(rows * H) : 0u));
     tma_load_1d(st, reinterpret_cast<const char*>(a.dy) + r * rowb, bb, &full[s], pol);
     tma_load_1d(st + L.off_h, reinterpret_cast<const char*>(a.h) + r * rowb, bb, &full[s], pol);
-    if (a.dh)
+    if constexpr (DH)
       tma_load_1d(st + L.off_dh, reinterpret_cast<const char*>(a.dh) + r * rowb, bb, &full[s], pol);
-    if (a.mask)
-      tma_load_1d(st + L.off_mask, a.mask + r * (int64_t)a.H, (uint32_t)(rows * a.H), &full[s], pol);
+    if constexpr (MASK)
+      tma_load_1d(st + L.off_mask, a.mask + r * (int64_t)H, (uint32_t)(rows * H), &full[s], pol);
   };
   const bool lead = producer && lr == 0;
   int issued = 0;
@@ -70,16 +73,21 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   grid_dep_launch_dependents();
   if (lead) {
     s_failed = 0;
-    for (int s = 0; s < L.nst; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], (uint32_t)(L.nrg * tpr));  // every consumer releases
+      mbar_init(&empty[s], (uint32_t)nthr_cons);  // every consumer releases
     }
     fence_mbar_init();
     // the first ring's worth of rows goes out before anything else happens
-    for (; issued < min(nstage, L.nst); ++issued) issue_stage(issued);
+    const uint64_t pol = policy_evict_first();
+    for (; issued < min(nstage, nst); ++issued) issue_stage(issued, pol);
   } else if (!producer) {
-    for (int i = threadIdx.x; i < a.nvec; i += nthr_cons)
-      sgam[i] = ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV);
+    for (int i = threadIdx.x; i < nvec; i += nthr_cons) {
+      float g[EV];
+      Act16<__nv_bfloat16>::unpack(ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV), g);
+      reinterpret_cast<float4*>(sgam)[2 * i] = make_float4(g[0], g[1], g[2], g[3]);
+      reinterpret_cast<float4*>(sgam)[2 * i + 1] = make_float4(g[4], g[5], g[6], g[7]);
+    }
   }
   __syncthreads();
 
@@ -97,73 +105,82 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
 
   if (producer) {
     if (lead) {
+      const uint64_t pol = policy_evict_first();
       for (int j = issued; j < nstage; ++j) {
-        const int k = j / L.nst;  // >= 1: the slot was used k times before
-        if (!mbar_wait(&empty[j % L.nst], (uint32_t)((k - 1) & 1))) {
+        const int k = j / nst;  // >= 1: the slot was used k times before
+        if (!mbar_wait(&empty[j % nst], (uint32_t)((k - 1) & 1))) {
           ok = false;
           break;
         }
-        issue_stage(j);
+        issue_stage(j, pol);
         issued = j + 1;
       }
       // nothing may still be landing in shared memory when the CTA exits
-      for (int j = max(0, issued - L.nst); j < issued; ++j)
-        mbar_wait(&full[j % L.nst], (uint32_t)((j / L.nst) & 1));
+      for (int j = max(0, issued - nst); j < issued; ++j)
+        mbar_wait(&full[j % nst], (uint32_t)((j / nst) & 1));
     }
   } else {
     float* rred = red + rg * 2 * (tpr >> 5) * NS;
     int slot = 0;
+    // the last vector slot of a thread may fall beyond the row
+    const bool last_in = lr + (VPT - 1) * tpr < nvec;
     // row statistics one row ahead, so their DRAM latency hides behind a row
     float rstd_n = 0.f, mu_n = 0.f;
     if (rg < n) {
       rstd_n = __ldcs(a.rstd + r0 + rg);
       if constexpr (LN) mu_n = __ldcs(a.mean + r0 + rg);
     }
+    const f2_t sc = f2(scale, scale);
     for (int j = 0; j < nstage; ++j) {
-      const int s = j % L.nst;
+      const int s = j % nst;
       // the whole row group agrees on the outcome of the wait before any of
       // it enters the row reduction's named barrier
       // (one-warp row groups vote; wider ones use their named barrier, id <= 8)
-      const bool landed = mbar_wait(&full[s], (uint32_t)((j / L.nst) & 1));
+      const bool landed = mbar_wait(&full[s], (uint32_t)((j / nst) & 1));
       const bool all_landed =
           tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
       if (!all_landed) {
         ok = false;
         break;
       }
-      const int i = j * L.nrg + rg;  // this row group's row of the stage
-      if (i >= n) {                  // last stage short of rows: just release it
+      const int i = j * nrg + rg;  // this row group's row of the stage
+      if (i >= n) {                // last stage short of rows: just release it
         mbar_arrive(&empty[s]);
         continue;
       }
       const unsigned char* st = stages + (size_t)s * L.stage_bytes;
-      const size_t rofs = (size_t)rg * a.H * 2;  // this row inside each tensor's block
+      const size_t rofs = (size_t)rg * rowb;  // this row inside each tensor's block
       const uint4* sdy = reinterpret_cast<const uint4*>(st + rofs);
       const uint4* sh = reinterpret_cast<const uint4*>(st + L.off_h + rofs);
       const uint4* sdh = reinterpret_cast<const uint4*>(st + L.off_dh + rofs);
-      const uint8_t* smk = st + L.off_mask + (size_t)rg * a.H;
+      const uint8_t* smk = st + L.off_mask + (size_t)rg * H;
       const int64_t r = r0 + i;
       const float rstd = rstd_n;
       const float mu = mu_n;
-      if (i + L.nrg < n) {
-        rstd_n = __ldcs(a.rstd + r + L.nrg);
-        if constexpr (LN) mu_n = __ldcs(a.mean + r + L.nrg);
+      if (i + nrg < n) {
+        rstd_n = __ldcs(a.rstd + r + nrg);
+        if constexpr (LN) mu_n = __ldcs(a.mean + r + nrg);
       }
       const f2_t r2 = f2(rstd, rstd), mu2 = f2(mu, mu);
 
-      // pass 1: row sums of g*xhat (and g), g = gamma*dy, xhat = (h-mu)*rstd
+      // pass 1: dy and xhat = (h-mu)*rstd to registers; row sums of g*xhat
+      // (and g), g = gamma*dy
+      f2_t dyk[VPT][4], xhk[VPT][4];
       f2_t sgx = f2(0.f, 0.f), sg = f2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int v = lr + k * tpr;
-        if (v < a.nvec) {
-          const uint4 wdy = sdy[v], wh = sh[v], wg = sgam[v];
+        if (k < VPT - 1 || last_in) {
+          const uint4 wdy = sdy[v], wh = sh[v];
+          const float4* gp = reinterpret_cast<const float4*>(sgam + v * EV);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const f2_t g = f2_mul(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wg)[q]),
-                                  bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]));
-            const f2_t xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]), mu2), r2);
-            sgx = f2_fma(g, xh, sgx);
+            const float4 g4 = gp[q >> 1];
+            const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
+            dyk[k][q] = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]);
+            xhk[k][q] = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]), mu2), r2);
+            const f2_t g = f2_mul(gm, dyk[k][q]);
+            sgx = f2_fma(g, xhk[k][q], sgx);
             if constexpr (LN) sg = f2_add(sg, g);
           }
         }
@@ -180,42 +197,48 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
       }
       row_allreduce<NS>(sums, tpr, lr, 1 + rg, rred, slot);
       slot ^= 1;
-      const f2_t ncgx = f2(-sums[0] / a.Hf, -sums[0] / a.Hf);
-      const float cgs = LN ? sums[NS - 1] / a.Hf : 0.f;
+      const f2_t ncgx = f2(-sums[0] * invH, -sums[0] * invH);
+      const float cgs = LN ? sums[NS - 1] * invH : 0.f;
       const f2_t cg = f2(cgs, cgs);
-      const f2_t sc = f2(a.scale, a.scale);
 
       // pass 2: dH, d_residual, d_sum; dgamma/dbeta contributions
+      __nv_bfloat16* dres_row = reinterpret_cast<__nv_bfloat16*>(a.d_res) + r * (int64_t)H;
+      __nv_bfloat16* dsum_row = reinterpret_cast<__nv_bfloat16*>(a.d_sum) + r * (int64_t)H;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int v = lr + k * tpr;
-        if (v < a.nvec) {
-          const uint4 wdy = sdy[v], wh = sh[v], wg = sgam[v];
-          const uint4 wdh = a.dh ? sdh[v] : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t mk = a.mask ? ld_mask_shared8(smk + v * EV) : 0xFFu;
+        if (k < VPT - 1 || last_in) {
+          const float4* gp = reinterpret_cast<const float4*>(sgam + v * EV);
+          uint4 wdh = make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (DH) wdh = sdh[v];
+          uint32_t mk = 0xFFu;
+          if constexpr (MASK) mk = ld_mask_shared8(smk + v * EV);
           uint32_t wres[4], wsum[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const f2_t dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]);
-            const f2_t g = f2_mul(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wg)[q]), dy);
-            const f2_t xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]), mu2), r2);
+            const float4 g4 = gp[q >> 1];
+            const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
+            const f2_t g = f2_mul(gm, dyk[k][q]);
             // rstd * (g - mean(g) - xhat * mean(g xhat)) + dh_out
-            const f2_t t = f2_fma(xh, ncgx, f2_sub(g, cg));
-            const f2_t dres = f2_fma(r2, t, bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdh)[q]));
+            const f2_t t = f2_fma(xhk[k][q], ncgx, f2_sub(g, cg));
+            f2_t dres;
+            if constexpr (DH)
+              dres = f2_fma(r2, t, bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdh)[q]));
+            else
+              dres = f2_mul(r2, t);
             f2_t dsum = f2_mul(dres, sc);
-            float sl, sh2;
-            f2_split(dsum, sl, sh2);
-            dsum = f2(((mk >> (2 * q)) & 1u) ? sl : 0.f, ((mk >> (2 * q + 1)) & 1u) ? sh2 : 0.f);
+            if constexpr (MASK) {
+              float sl, sh2;
+              f2_split(dsum, sl, sh2);
+              dsum = f2(((mk >> (2 * q)) & 1u) ? sl : 0.f, ((mk >> (2 * q + 1)) & 1u) ? sh2 : 0.f);
+            }
             wres[q] = f2_to_bf2(dres);
             wsum[q] = f2_to_bf2(dsum);
-            dg[k][q] = f2_fma(dy, xh, dg[k][q]);
-            if constexpr (LN) db[k][q] = f2_add(db[k][q], dy);
+            dg[k][q] = f2_fma(dyk[k][q], xhk[k][q], dg[k][q]);
+            if constexpr (LN) db[k][q] = f2_add(db[k][q], dyk[k][q]);
           }
-          const int64_t o = r * (int64_t)a.H + (int64_t)v * EV;
-          st_stream(reinterpret_cast<__nv_bfloat16*>(a.d_res) + o,
-                    make_uint4(wres[0], wres[1], wres[2], wres[3]));
-          st_stream(reinterpret_cast<__nv_bfloat16*>(a.d_sum) + o,
-                    make_uint4(wsum[0], wsum[1], wsum[2], wsum[3]));
+          st_stream(dres_row + v * EV, make_uint4(wres[0], wres[1], wres[2], wres[3]));
+          st_stream(dsum_row + v * EV, make_uint4(wsum[0], wsum[1], wsum[2], wsum[3]));
         }
       }
       mbar_arrive(&empty[s]);
@@ -231,8 +254,8 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lr + k * tpr;
-      if (v < a.nvec) {
-        float* dst = part + (size_t)rg * NS * a.H + v * EV;
+      if (v < nvec) {
+        float* dst = part + (size_t)rg * NS * H + v * EV;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float lo, hi;
@@ -241,8 +264,8 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
           dst[2 * q + 1] = hi;
           if constexpr (LN) {
             f2_split(db[k][q], lo, hi);
-            dst[a.H + 2 * q] = lo;
-            dst[a.H + 2 * q + 1] = hi;
+            dst[H + 2 * q] = lo;
+            dst[H + 2 * q + 1] = hi;
           }
         }
       }
@@ -251,11 +274,11 @@ __global__ void __launch_bounds__(544, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   __syncthreads();
   // a CTA whose wait timed out poisons its partial so dgamma/dbeta are NaN
   const bool failed = s_failed != 0;
-  for (int c = threadIdx.x; c < NS * a.H; c += blockDim.x) {
+  for (int c = threadIdx.x; c < NS * H; c += blockDim.x) {
     float acc = part[c];
-    for (int g = 1; g < L.nrg; ++g) acc += part[(size_t)g * NS * a.H + c];
-    const int st = c / a.H;
-    __stcg(a.ws + ((int64_t)st * a.nparts + blockIdx.x) * a.H + (c - st * a.H),
+    for (int g = 1; g < nrg; ++g) acc += part[(size_t)g * NS * H + c];
+    const int st = c / H;
+    __stcg(a.ws + ((int64_t)st * a.nparts + blockIdx.x) * H + (c - st * H),
            failed ? __int_as_float(0x7FC00000) : acc);
   }
 }

@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
   float* sgb = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // gamma[H], beta[H]
   unsigned char* stages = dsm + L.smem_stages;
 
-  const int tpr = a.tpr;
+  const int H = a.H, nvec = a.nvec, tpr = a.tpr;
+  const float invH = 1.0f / a.Hf;
   const int nthr_cons = L.nrg * tpr;
   const bool producer = threadIdx.x >= nthr_cons;
   const int rg = producer ? L.nrg : (int)threadIdx.x / tpr;
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
   const int64_t r1 = min(a.rows, r0 + L.rows_per_cta);
   const int n = r1 > r0 ? (int)(r1 - r0) : 0;
   const int nstage = (n + L.nrg - 1) / L.nrg;
-  const size_t rowb = (size_t)a.H * 2;
+  const size_t rowb = (size_t)H * 2;
   const uint64_t pol = policy_evict_first();
 
   auto issue_stage = [&](int j) {
@@ -134,6 +135,8 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
 
   float* rred = red + rg * 2 * (tpr >> 5);
   const f2_t shi = f2(a.scale, a.scale), slo = f2(a.scale_lo, a.scale_lo);
+  const bool dropout = a.dropout != 0, nontie = a.dropout && !a.dyadic_scale;
+  const bool last_in = lr + (VPT - 1) * tpr < nvec;  // the last vector slot may fall outside
   for (int j = 0; j < nstage; ++j) {
     const int s = j % L.nst;
     const bool landed = mbar_wait(&full[s], (uint32_t)((j / L.nst) & 1));
@@ -152,6 +155,9 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
     const unsigned char* st = stages + (size_t)s * L.stage_bytes + (size_t)rg * rowb;
     const int64_t r = r0 + i;
     const int64_t grow = a.grow0 + r;
+    __nv_bfloat16* h_row = reinterpret_cast<__nv_bfloat16*>(a.h) + r * (int64_t)H;
+    __nv_bfloat16* y_row = reinterpret_cast<__nv_bfloat16*>(a.y) + r * (int64_t)H;
+    uint8_t* m_row = a.mask ? a.mask + r * (int64_t)H : nullptr;
 
     // ---- reduce, mask, dropout, residual add; store h and the mask --------
     f2_t hf[VPT][4];
@@ -159,14 +165,14 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lr + k * tpr;
-      if (v < a.nvec) {
+      if (k < VPT - 1 || last_in) {
         uint4 pw[T];
 #pragma unroll
         for (int t = 0; t < T; ++t) pw[t] = reinterpret_cast<const uint4*>(st + (size_t)t * L.blk)[v];
         const uint4 rw = reinterpret_cast<const uint4*>(st + (size_t)T * L.blk)[v];
-        const uint64_t g0 = (uint64_t)(grow * a.H + (int64_t)v * EV);
+        const uint64_t g0 = (uint64_t)(grow * H + (int64_t)v * EV);
         uint32_t keep = 0xFFu;
-        if (a.dropout)
+        if (dropout)
           keep = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
         uint32_t hw[4];
 #pragma unroll
@@ -176,19 +182,17 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
           for (int t = 1; t < T; ++t)
             acc = f2_add(acc, bf2_to_f2(reinterpret_cast<const uint32_t*>(&pw[t])[q]));
           const f2_t res = bf2_to_f2(reinterpret_cast<const uint32_t*>(&rw)[q]);
-          if (a.dropout) {
+          if (dropout) {
             float al, ah;
             f2_split(acc, al, ah);
             acc = f2(((keep >> (2 * q)) & 1u) ? al : 0.f, ((keep >> (2 * q + 1)) & 1u) ? ah : 0.f);
           }
-          hw[q] = (a.dropout && !a.dyadic_scale) ? residual_bf2_drop(res, acc, shi, slo)
-                                                 : residual_bf2(res, acc, shi, slo);
+          hw[q] = nontie ? residual_bf2_drop(res, acc, shi, slo) : residual_bf2(res, acc, shi, slo);
           hf[k][q] = bf2_to_f2(hw[q]);
           s2 = LN ? f2_add(s2, hf[k][q]) : f2_fma(hf[k][q], hf[k][q], s2);
         }
-        const int64_t o = r * (int64_t)a.H + (int64_t)v * EV;
-        st_stream(reinterpret_cast<__nv_bfloat16*>(a.h) + o, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-        if (a.mask) st_mask<EV>(a.mask + o, keep);
+        st_stream(h_row + v * EV, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+        if (m_row) st_mask<EV>(m_row + v * EV, keep);
       }
     }
     mbar_arrive(&empty[s]);  // the stage is no longer read
@@ -203,12 +207,12 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
     row_allreduce<1>(sv, tpr, lr, 1 + rg, rred, 0);
     float mu = 0.f, rstd;
     if constexpr (LN) {
-      mu = sv[0] / a.Hf;
+      mu = sv[0] * invH;
       const f2_t mu2 = f2(mu, mu);
       f2_t q2 = f2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
-        if (lr + k * tpr < a.nvec) {
+        if (k < VPT - 1 || last_in) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const f2_t dd = f2_sub(hf[k][q], mu2);
@@ -223,9 +227,9 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
         qv[0] = lo + hi;
       }
       row_allreduce<1>(qv, tpr, lr, 1 + rg, rred, 1);
-      rstd = 1.0f / sqrtf(qv[0] / a.Hf + a.eps);
+      rstd = 1.0f / sqrtf(qv[0] * invH + a.eps);
     } else {
-      rstd = 1.0f / sqrtf(sv[0] / a.Hf + a.eps);
+      rstd = 1.0f / sqrtf(sv[0] * invH + a.eps);
     }
 
     // ---- y = gamma * xhat (+ beta), one rounding ------------------------------
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lr + k * tpr;
-      if (v < a.nvec) {
+      if (k < VPT - 1 || last_in) {
         const float4* gp = reinterpret_cast<const float4*>(sgb + v * EV);
         uint32_t yw[4];
 #pragma unroll
@@ -241,7 +245,7 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
           const float4 g4 = gp[q2];
           const f2_t ga = f2(g4.x, g4.y), gb = f2(g4.z, g4.w);
           if constexpr (LN) {
-            const float4 b4 = reinterpret_cast<const float4*>(sgb + a.H + v * EV)[q2];
+            const float4 b4 = reinterpret_cast<const float4*>(sgb + H + v * EV)[q2];
             yw[2 * q2] = f2_to_bf2(f2_fma(ga, f2_mul(f2_sub(hf[k][2 * q2], mu2), r2), f2(b4.x, b4.y)));
             yw[2 * q2 + 1] =
                 f2_to_bf2(f2_fma(gb, f2_mul(f2_sub(hf[k][2 * q2 + 1], mu2), r2), f2(b4.z, b4.w)));
@@ -250,8 +254,7 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
             yw[2 * q2 + 1] = f2_to_bf2(f2_mul(gb, f2_mul(hf[k][2 * q2 + 1], r2)));
           }
         }
-        st_stream(reinterpret_cast<__nv_bfloat16*>(a.y) + r * (int64_t)a.H + (int64_t)v * EV,
-                  make_uint4(yw[0], yw[1], yw[2], yw[3]));
+        st_stream(y_row + v * EV, make_uint4(yw[0], yw[1], yw[2], yw[3]));
       }
     }
     if (lr == 0) {
