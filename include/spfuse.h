@@ -207,6 +207,10 @@ sp_status_t hp2sp(const void* in, void* out, int64_t N, int64_t H, int32_t T,
 /* Static string for a status code. */
 const char* sp_status_string(sp_status_t status);
 
+/* Text of the CUDA error behind the most recent SP_ERR_CUDA returned to the
+ * calling host thread ("no error" if there was none). */
+const char* sp_last_cuda_error(void);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t sp_version(void);
 

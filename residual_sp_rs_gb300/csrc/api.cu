@@ -28,6 +28,15 @@ bool inject_launch_failure() {
   return on;
 }
 
+// The CUDA error behind the last SP_ERR_CUDA on this host thread.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+sp_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return SP_OK;
+  g_last_cuda_error = e;
+  return SP_ERR_CUDA;
+}
+
 struct Problem {
   int T, j, nshards, dtype, norm;
   int64_t S, B, H, R, rows;
@@ -103,10 +112,11 @@ sp_status_t plan_bwd(const Problem& pr, bool has_dh, bool has_mask, BwdPlan* pl)
   pl->tma = false;
   if (pr.dtype == SP_BF16) {
     int dev = 0, sms = 0, optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      return SP_ERR_CUDA;
+    cudaError_t qe = cudaGetDevice(&dev);
+    if (qe == cudaSuccess) qe = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (qe == cudaSuccess)
+      qe = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (qe != cudaSuccess) return from_cuda(qe);
     BwdTmaPlan probe;
     if (plan_bwd_tma(pr.H, ln, true, true, optin, &probe)) {
       pl->tma = true;
@@ -139,7 +149,6 @@ sp_status_t plan_bwd(const Problem& pr, bool has_dh, bool has_mask, BwdPlan* pl)
   return SP_OK;
 }
 
-sp_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SP_OK : SP_ERR_CUDA; }
 
 }  // namespace
 }  // namespace spf
@@ -202,10 +211,11 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (pr.dtype == SP_BF16) {
     int dev = 0, sms = 0, optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      return SP_ERR_CUDA;
+    cudaError_t qe = cudaGetDevice(&dev);
+    if (qe == cudaSuccess) qe = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (qe == cudaSuccess)
+      qe = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (qe != cudaSuccess) return from_cuda(qe);
     FwdTmaPlan tp;
     if (plan_fwd_tma(pr.H, pr.T, ln, optin, pr.rows, sms, &tp)) {
       a.tpr = tp.shape.tpr;
@@ -294,7 +304,7 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc, const void
     } else {
       e = launch_bwd(pr.dtype, ln, a, pl.shape, dim3((unsigned)pl.ctas), pl.smem, cs);
     }
-    if (e != cudaSuccess) return SP_ERR_CUDA;
+    if (e != cudaSuccess) return from_cuda(e);
     nparts = pl.nparts;
   }
   return from_cuda(launch_colsum(ws, nparts, (int)pr.H, ln, dgamma, ln ? dbeta : nullptr, cs));
@@ -340,5 +350,7 @@ const char* sp_status_string(sp_status_t s) {
 }
 
 int32_t sp_version(void) { return 100; }
+
+const char* sp_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 }  // extern "C"

@@ -14,6 +14,9 @@ void (*tma_kernel_v(int vpt))(const BwdArgs, const BwdTmaLayout) {
     case 3:
       if constexpr (!LN) return sp_bwd_tma_kernel<LN, 3, DH, MASK>;  // LayerNorm stays <= 2
       return nullptr;
+    case 4:
+      if constexpr (!LN) return sp_bwd_tma_kernel<LN, 4, DH, MASK>;
+      return nullptr;
     default: return nullptr;
   }
 }
@@ -25,18 +28,19 @@ void (*tma_kernel(int vpt, bool dh, bool mask))(const BwdArgs, const BwdTmaLayou
 }
 
 constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, rounded up
-constexpr int kBwdTmaConsumers = 512;  // consumer threads per CTA
+constexpr int kBwdTmaConsumers = 480;  // consumer threads per CTA (+1 producer warp: 16 warps)
 
 }  // namespace
 
 bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, BwdTmaPlan* p) {
   if (H % 16 != 0) return false;  // mask rows must be whole 16-byte copies
   const int nvec = (int)(H / 8);
-  // 16 consumer warps; a row group of tpr threads holds <= 3 vectors per
-  // thread (<= 2 for LayerNorm, whose dbeta accumulators add registers)
-  const int vcap = ln ? 2 : 3;
+  // up to 15 consumer warps; a row group of tpr (<= 256) threads holds <= 4
+  // vectors per thread (<= 2 for LayerNorm, whose dbeta accumulators add
+  // registers)
+  const int vcap = ln ? 2 : 4;
   int tpr = 32;
-  while (tpr < kBwdTmaConsumers && (nvec + tpr - 1) / tpr > vcap) tpr *= 2;
+  while (tpr < 256 && (nvec + tpr - 1) / tpr > vcap) tpr *= 2;
   const int vpt = (nvec + tpr - 1) / tpr;
   if (vpt > vcap) return false;
   int nrg = kBwdTmaConsumers / tpr;  // rows per stage, one per row group

@@ -26,8 +26,13 @@
 
 namespace spf {
 
+// At most 16 warps (15 consumer + 1 producer), so 128 registers per thread fit
+// every SM sub-partition's register file.  KEEP: dy and xhat stay in registers
+// between the two passes (VPT <= 3); with 4 vectors per thread pass 2 reads
+// them from shared memory again instead.
 template <bool LN, int VPT, bool DH, bool MASK>
-__global__ void __maxnreg__(120) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
+__global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
+  constexpr bool KEEP = VPT <= 3;
   constexpr int EV = 8;
   constexpr int NS = LN ? 2 : 1;
   __shared__ float red[2 * 32 * 2];
@@ -165,7 +170,7 @@ __global__ void __maxnreg__(120) sp_bwd_tma_kernel(const BwdArgs a, const BwdTma
 
       // pass 1: dy and xhat = (h-mu)*rstd to registers; row sums of g*xhat
       // (and g), g = gamma*dy
-      f2_t dyk[VPT][4], xhk[VPT][4];
+      f2_t dyk[KEEP ? VPT : 1][4], xhk[KEEP ? VPT : 1][4];
       f2_t sgx = f2(0.f, 0.f), sg = f2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -177,10 +182,14 @@ __global__ void __maxnreg__(120) sp_bwd_tma_kernel(const BwdArgs a, const BwdTma
           for (int q = 0; q < 4; ++q) {
             const float4 g4 = gp[q >> 1];
             const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
-            dyk[k][q] = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]);
-            xhk[k][q] = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]), mu2), r2);
-            const f2_t g = f2_mul(gm, dyk[k][q]);
-            sgx = f2_fma(g, xhk[k][q], sgx);
+            const f2_t dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]);
+            const f2_t xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]), mu2), r2);
+            if constexpr (KEEP) {
+              dyk[k][q] = dy;
+              xhk[k][q] = xh;
+            }
+            const f2_t g = f2_mul(gm, dy);
+            sgx = f2_fma(g, xh, sgx);
             if constexpr (LN) sg = f2_add(sg, g);
           }
         }
@@ -213,14 +222,27 @@ __global__ void __maxnreg__(120) sp_bwd_tma_kernel(const BwdArgs a, const BwdTma
           if constexpr (DH) wdh = sdh[v];
           uint32_t mk = 0xFFu;
           if constexpr (MASK) mk = ld_mask_shared8(smk + v * EV);
+          uint4 wdy2 = make_uint4(0u, 0u, 0u, 0u), wh2 = make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (!KEEP) {
+            wdy2 = sdy[v];
+            wh2 = sh[v];
+          }
           uint32_t wres[4], wsum[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const float4 g4 = gp[q >> 1];
             const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
-            const f2_t g = f2_mul(gm, dyk[k][q]);
+            f2_t dy, xh;
+            if constexpr (KEEP) {
+              dy = dyk[k][q];
+              xh = xhk[k][q];
+            } else {
+              dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy2)[q]);
+              xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh2)[q]), mu2), r2);
+            }
+            const f2_t g = f2_mul(gm, dy);
             // rstd * (g - mean(g) - xhat * mean(g xhat)) + dh_out
-            const f2_t t = f2_fma(xhk[k][q], ncgx, f2_sub(g, cg));
+            const f2_t t = f2_fma(xh, ncgx, f2_sub(g, cg));
             f2_t dres;
             if constexpr (DH)
               dres = f2_fma(r2, t, bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdh)[q]));
@@ -234,8 +256,8 @@ __global__ void __maxnreg__(120) sp_bwd_tma_kernel(const BwdArgs a, const BwdTma
             }
             wres[q] = f2_to_bf2(dres);
             wsum[q] = f2_to_bf2(dsum);
-            dg[k][q] = f2_fma(dyk[k][q], xhk[k][q], dg[k][q]);
-            if constexpr (LN) db[k][q] = f2_add(db[k][q], dyk[k][q]);
+            dg[k][q] = f2_fma(dy, xh, dg[k][q]);
+            if constexpr (LN) db[k][q] = f2_add(db[k][q], dy);
           }
           st_stream(dres_row + v * EV, make_uint4(wres[0], wres[1], wres[2], wres[3]));
           st_stream(dsum_row + v * EV, make_uint4(wsum[0], wsum[1], wsum[2], wsum[3]));

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.sp_status_string.argtypes = [ctypes.c_int]
         L.sp_version.restype = ctypes.c_int32
         L.sp_version.argtypes = []
+        L.sp_last_cuda_error.restype = ctypes.c_char_p
+        L.sp_last_cuda_error.argtypes = []
         _lib = L
     return _lib
 
@@ -101,7 +103,10 @@ def _stream(stream):
 
 def _check(code: int):
     if code != 0:
-        raise RuntimeError(lib().sp_status_string(code).decode())
+        msg = lib().sp_status_string(code).decode()
+        if code == 6:  # SP_ERR_CUDA
+            msg += f" ({lib().sp_last_cuda_error().decode()})"
+        raise RuntimeError(msg)
 
 
 def status_string(code: int) -> str:
