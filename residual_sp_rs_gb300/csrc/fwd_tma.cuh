@@ -55,7 +55,50 @@ __device__ __forceinline__ uint32_t residual_bf2_drop(f2_t res, f2_t acc, f2_t s
   return w;
 }
 
-template <int T, bool LN, int VPT>
+// The same rounding for one 16-byte vector (four pairs) with a single guard
+// branch for the vector instead of one per pair.
+__device__ __forceinline__ void residual_vec8_drop(const f2_t (&acc)[4], const f2_t (&res)[4], f2_t s_hi,
+                                                   f2_t s_lo, uint32_t (&hw)[4]) {
+  bool risky = false;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const f2_t h1 = f2_fma(acc[q], s_hi, res[q]);
+    float h1l, h1h;
+    f2_split(h1, h1l, h1h);
+    const uint32_t ul = __float_as_uint(h1l), uh = __float_as_uint(h1h);
+    const f2_t m = f2(__uint_as_float((ul & 0xFFFF0000u) | 0x8000u),
+                      __uint_as_float((uh & 0xFFFF0000u) | 0x8000u));
+    const f2_t d = f2_fma(acc[q], s_lo, f2_fma(acc[q], s_hi, f2_sub(res[q], m)));
+    const f2_t gap = f2_mul(h1, f2(0x1p12f, 0x1p12f));
+    float dl, dh, gl, gh, rl, rh;
+    f2_split(d, dl, dh);
+    f2_split(gap, gl, gh);
+    f2_split(res[q], rl, rh);
+    const uint32_t pl = (int)(__float_as_uint(dl) ^ (ul & 0x80000000u)) > 0 ? 0x1u : 0u;
+    const uint32_t ph = (int)(__float_as_uint(dh) ^ (uh & 0x80000000u)) > 0 ? 0x10000u : 0u;
+    hw[q] = __byte_perm(ul, uh, 0x7632) + pl + ph;
+    risky |= (fabsf(gl) < fabsf(rl)) | (fabsf(gh) < fabsf(rh));
+  }
+  if (risky) {  // rare: |h| < 2^-12 |res| somewhere in the vector
+    float shl, shh, sll, slh;
+    f2_split(s_hi, shl, shh);
+    f2_split(s_lo, sll, slh);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float al, ah, rl, rh;
+      f2_split(acc[q], al, ah);
+      f2_split(res[q], rl, rh);
+      uint32_t bl = hw[q] & 0xFFFFu, bh = hw[q] >> 16;
+      if (fabsf(__fmaf_rn(al, shl, rl)) * 0x1p12f < fabsf(rl)) bl = residual_bf16_dd(rl, al, shl, sll, true);
+      if (fabsf(__fmaf_rn(ah, shh, rh)) * 0x1p12f < fabsf(rh)) bh = residual_bf16_dd(rh, ah, shh, slh, true);
+      hw[q] = bl | (bh << 16);
+    }
+  }
+}
+
+// FAST: p > 0 with 1/(1-p) not dyadic (the common case) -- no tie rule, no
+// runtime mode branches in the element loop.  Otherwise GENERIC.
+template <int T, bool LN, int VPT, bool FAST>
 __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, const FwdTmaLayout L) {
   constexpr int EV = 8;
   __shared__ float red[2 * 32 * 2];
@@ -172,9 +215,29 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
         const uint4 rw = reinterpret_cast<const uint4*>(st + (size_t)T * L.blk)[v];
         const uint64_t g0 = (uint64_t)(grow * H + (int64_t)v * EV);
         uint32_t keep = 0xFFu;
-        if (dropout)
+        if (FAST || dropout)
           keep = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
         uint32_t hw[4];
+        if constexpr (FAST) {
+          f2_t acc[4], res[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[q] = bf2_to_f2(reinterpret_cast<const uint32_t*>(&pw[0])[q]);
+#pragma unroll
+            for (int t = 1; t < T; ++t)
+              acc[q] = f2_add(acc[q], bf2_to_f2(reinterpret_cast<const uint32_t*>(&pw[t])[q]));
+            float al, ah;
+            f2_split(acc[q], al, ah);
+            acc[q] = f2(((keep >> (2 * q)) & 1u) ? al : 0.f, ((keep >> (2 * q + 1)) & 1u) ? ah : 0.f);
+            res[q] = bf2_to_f2(reinterpret_cast<const uint32_t*>(&rw)[q]);
+          }
+          residual_vec8_drop(acc, res, shi, slo, hw);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            hf[k][q] = bf2_to_f2(hw[q]);
+            s2 = LN ? f2_add(s2, hf[k][q]) : f2_fma(hf[k][q], hf[k][q], s2);
+          }
+        } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           f2_t acc = bf2_to_f2(reinterpret_cast<const uint32_t*>(&pw[0])[q]);
@@ -190,6 +253,7 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
           hw[q] = nontie ? residual_bf2_drop(res, acc, shi, slo) : residual_bf2(res, acc, shi, slo);
           hf[k][q] = bf2_to_f2(hw[q]);
           s2 = LN ? f2_add(s2, hf[k][q]) : f2_fma(hf[k][q], hf[k][q], s2);
+        }
         }
         st_stream(h_row + v * EV, make_uint4(hw[0], hw[1], hw[2], hw[3]));
         if (m_row) st_mask<EV>(m_row + v * EV, keep);

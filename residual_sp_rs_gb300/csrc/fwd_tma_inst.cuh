@@ -1,5 +1,5 @@
 // fwd_tma_inst.cuh -- instances of the TMA-fed forward for one norm over
-// T = 1..8 and VPT = 1..4.
+// T = 1..8, VPT = 1..3 and the fast / generic rounding mode.
 #pragma once
 
 #include "fwd_tma.cuh"
@@ -7,30 +7,35 @@
 
 namespace spf {
 
-template <bool LN, int T>
+template <bool LN, int T, bool FAST>
 inline void (*fwd_tma_kernel_for_vpt(int vpt))(const FwdArgs, const FwdTmaLayout) {
   switch (vpt) {
-    case 1: return sp_fwd_tma_kernel<T, LN, 1>;
-    case 2: return sp_fwd_tma_kernel<T, LN, 2>;
-    case 3: return sp_fwd_tma_kernel<T, LN, 3>;
-    case 4: return sp_fwd_tma_kernel<T, LN, 4>;
+    case 1: return sp_fwd_tma_kernel<T, LN, 1, FAST>;
+    case 2: return sp_fwd_tma_kernel<T, LN, 2, FAST>;
+    case 3: return sp_fwd_tma_kernel<T, LN, 3, FAST>;
     default: return nullptr;
   }
+}
+
+template <bool LN, int T>
+inline void (*fwd_tma_kernel_for(int vpt, bool fast))(const FwdArgs, const FwdTmaLayout) {
+  return fast ? fwd_tma_kernel_for_vpt<LN, T, true>(vpt) : fwd_tma_kernel_for_vpt<LN, T, false>(vpt);
 }
 
 template <bool LN>
 cudaError_t launch_fwd_tma_impl(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid,
                                 cudaStream_t st) {
   void (*k)(const FwdArgs, const FwdTmaLayout) = nullptr;
+  const bool fast = a.dropout && !a.dyadic_scale;
   switch (T) {
-    case 1: k = fwd_tma_kernel_for_vpt<LN, 1>(p.shape.vpt); break;
-    case 2: k = fwd_tma_kernel_for_vpt<LN, 2>(p.shape.vpt); break;
-    case 3: k = fwd_tma_kernel_for_vpt<LN, 3>(p.shape.vpt); break;
-    case 4: k = fwd_tma_kernel_for_vpt<LN, 4>(p.shape.vpt); break;
-    case 5: k = fwd_tma_kernel_for_vpt<LN, 5>(p.shape.vpt); break;
-    case 6: k = fwd_tma_kernel_for_vpt<LN, 6>(p.shape.vpt); break;
-    case 7: k = fwd_tma_kernel_for_vpt<LN, 7>(p.shape.vpt); break;
-    case 8: k = fwd_tma_kernel_for_vpt<LN, 8>(p.shape.vpt); break;
+    case 1: k = fwd_tma_kernel_for<LN, 1>(p.shape.vpt, fast); break;
+    case 2: k = fwd_tma_kernel_for<LN, 2>(p.shape.vpt, fast); break;
+    case 3: k = fwd_tma_kernel_for<LN, 3>(p.shape.vpt, fast); break;
+    case 4: k = fwd_tma_kernel_for<LN, 4>(p.shape.vpt, fast); break;
+    case 5: k = fwd_tma_kernel_for<LN, 5>(p.shape.vpt, fast); break;
+    case 6: k = fwd_tma_kernel_for<LN, 6>(p.shape.vpt, fast); break;
+    case 7: k = fwd_tma_kernel_for<LN, 7>(p.shape.vpt, fast); break;
+    case 8: k = fwd_tma_kernel_for<LN, 8>(p.shape.vpt, fast); break;
     default: break;
   }
   if (!k) return cudaErrorInvalidValue;

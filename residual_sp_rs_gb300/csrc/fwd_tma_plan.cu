@@ -8,7 +8,7 @@ constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, roun
 constexpr int kMaxConsumers = 512;
 }  // namespace
 
-// Picks the row-group width (<= 4 vectors per thread) and rows per stage that
+// Picks the row-group width (<= 3 vectors per thread) and rows per stage that
 // give the most consumer threads while at least two stages fit in shared
 // memory next to gamma/beta; false when no such ring exists (long rows).
 bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms, FwdTmaPlan* p) {
@@ -20,7 +20,7 @@ bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms
   int best_threads = 0;
   for (int tpr = 32; tpr <= kMaxConsumers; tpr *= 2) {
     const int vpt = (nvec + tpr - 1) / tpr;
-    if (vpt > 4) continue;
+    if (vpt > 3) continue;
     for (int nrg = kMaxConsumers / tpr; nrg >= 1; nrg /= 2) {
       if (tpr > 32 && nrg > 15) continue;  // named barriers 1..nrg
       const size_t blk = (size_t)nrg * rowb;
