@@ -76,6 +76,27 @@ def layout_bytes(w, rows):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (one process per GPU, the same workload on each)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: the job is done when every rank is."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tokens_per_s(tokens_per_step: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank processed `steps` steps of its own
+    batch in at most `ms` milliseconds."""
+    return tokens_per_step * steps * world / (ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 
@@ -251,14 +272,9 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_per_step = ms / args.steps
-    tokens = rows * args.steps * world
-    value = tokens / (ms / 1e3)
+    value = weak_scaling_tokens_per_s(rows, args.steps, world, ms)
     step_bytes = fwd_bytes(w, rows) + bwd_bytes(w, rows) + 2 * layout_bytes(w, rows)
     step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
 
