@@ -99,7 +99,8 @@ typedef struct sp_rs_desc_t {
  * residual : [nshards*R, H] residual stream of those shards.
  * gamma    : [H]; beta: [H] for LayerNorm (ignored for RMSNorm).
  * h_out, y_out : [nshards*R, H] outputs (residual stream, norm output).
- * mask_out : [nshards*R, H] bytes (0/1); may be NULL only when p == 0.
+ * mask_out : [nshards*R, H] bytes (0/1), or NULL: then the mask is not
+ *            stored and the backward regenerates it from the seed.
  * rstd_out : [nshards*R] fp32.  mean_out: [nshards*R] fp32, LayerNorm only
  *            (ignored for RMSNorm).
  * Alignment: activation pointers and mask 16 bytes; rstd/mean 4 bytes.
@@ -137,7 +138,11 @@ size_t sp_rs_bwd_workspace_bytes(const sp_rs_desc_t* desc);
  *   nshards = T performs in place.  Deterministic two-pass reduction.
  *
  * dy, dh_out, h_saved : [nshards*R, H]; gamma: [H]; mask: [nshards*R, H]
- * bytes (NULL iff p == 0); rstd, mean: [nshards*R] as written by the forward
+ * bytes as written by the forward, or NULL: with p > 0 the keep decisions
+ * are then recomputed from desc->seed and the global element index -- the
+ * same generator stream, so bit-identical to a stored mask -- trading
+ * 2 bytes per element of mask traffic (forward write, backward read) for
+ * the generator's arithmetic; rstd, mean: [nshards*R] as written by the forward
  * (mean ignored for RMSNorm).  d_residual, d_sum: [nshards*R, H] outputs;
  * dgamma, dbeta: [H] fp32 outputs (dbeta ignored for RMSNorm).
  * workspace: device scratch of at least sp_rs_bwd_workspace_bytes(desc)

@@ -169,7 +169,6 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   if (pr.rows == 0) return SP_OK;  // nothing to read or write
   if (!partials || !residual || !gamma || !h_out || !y_out || !rstd_out) return SP_ERR_INVALID_ARG;
   if (ln && (!beta || !mean_out)) return SP_ERR_INVALID_ARG;
-  if (desc->p > 0.0f && !mask_out) return SP_ERR_INVALID_ARG;
   for (int t = 0; t < pr.T; ++t) {
     if (!partials[t]) return SP_ERR_INVALID_ARG;
     if (!aligned(partials[t], 16)) return SP_ERR_ALIGN;
@@ -261,14 +260,13 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc, const void
   if (!empty && (!dy || !h_saved || !gamma || !rstd || !d_residual || !d_sum))
     return SP_ERR_INVALID_ARG;
   if (!empty && ln && !mean) return SP_ERR_INVALID_ARG;
-  if (!empty && desc->p > 0.0f && !mask) return SP_ERR_INVALID_ARG;
   if (!aligned(dy, 16) || (dh_out && !aligned(dh_out, 16)) || !aligned(h_saved, 16) ||
       !aligned(gamma, 16) || (mask && !aligned(mask, 16)) || !aligned(rstd, 4) ||
       (ln && !aligned(mean, 4)) || !aligned(d_residual, 16) || !aligned(d_sum, 16) ||
       !aligned(dgamma, 16) || (ln && !aligned(dbeta, 16)))
     return SP_ERR_ALIGN;
   BwdPlan pl;
-  st = plan_bwd(pr, dh_out != nullptr, desc->p > 0.0f, &pl);
+  st = plan_bwd(pr, dh_out != nullptr, desc->p > 0.0f && mask != nullptr, &pl);
   if (st != SP_OK) return st;
   if (!workspace || workspace_bytes < pl.ws_bytes) return SP_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return SP_ERR_ALIGN;
@@ -284,6 +282,13 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc, const void
     a.h = h_saved;
     a.gamma = gamma;
     a.mask = desc->p > 0.0f ? mask : nullptr;
+    a.regen = desc->p > 0.0f && !mask ? 1 : 0;
+    a.thr = (uint32_t)std::floor((double)desc->p * 4294967296.0);
+    a.grow0 = (int64_t)pr.j * pr.R;
+    for (int i = 0; i < 10; ++i) {
+      a.keys.rk[2 * i] = (uint32_t)desc->seed + (uint32_t)i * 0x9E3779B9u;
+      a.keys.rk[2 * i + 1] = (uint32_t)(desc->seed >> 32) + (uint32_t)i * 0xBB67AE85u;
+    }
     a.rstd = rstd;
     a.mean = ln ? mean : nullptr;
     a.d_res = d_residual;

@@ -77,7 +77,15 @@ __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
         dyv[k] = ld_stream(reinterpret_cast<const Act*>(a.dy) + o);
         hv[k] = ld_stream(reinterpret_cast<const Act*>(a.h) + o);
         dhv[k] = a.dh ? ld_stream(reinterpret_cast<const Act*>(a.dh) + o) : make_uint4(0u, 0u, 0u, 0u);
-        mk[k] = a.mask ? ld_mask<EV>(a.mask + o) : (1u << EV) - 1u;
+        if (a.mask) {
+          mk[k] = ld_mask<EV>(a.mask + o);
+        } else if (a.regen) {  // the forward's keep bits, from the same generator
+          const uint64_t g0 = (uint64_t)((a.grow0 + r) * (int64_t)a.H + (int64_t)v * EV);
+          mk[k] = keep_bits4(g0 >> 2, a.keys, a.thr);
+          if constexpr (EV == 8) mk[k] |= keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4;
+        } else {
+          mk[k] = (1u << EV) - 1u;
+        }
       }
     }
     const float rstd = __ldcs(a.rstd + r);

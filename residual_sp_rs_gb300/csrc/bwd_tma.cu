@@ -6,25 +6,32 @@ namespace spf {
 
 namespace {
 
-template <bool LN, bool DH, bool MASK>
+template <bool LN, bool DH, bool MASK, bool REGEN>
 void (*tma_kernel_v(int vpt))(const BwdArgs, const BwdTmaLayout) {
   switch (vpt) {
-    case 1: return sp_bwd_tma_kernel<LN, 1, DH, MASK>;
-    case 2: return sp_bwd_tma_kernel<LN, 2, DH, MASK>;
+    case 1: return sp_bwd_tma_kernel<LN, 1, DH, MASK, REGEN>;
+    case 2: return sp_bwd_tma_kernel<LN, 2, DH, MASK, REGEN>;
     case 3:
-      if constexpr (!LN) return sp_bwd_tma_kernel<LN, 3, DH, MASK>;  // LayerNorm stays <= 2
+      if constexpr (!LN) return sp_bwd_tma_kernel<LN, 3, DH, MASK, REGEN>;  // LayerNorm stays <= 2
       return nullptr;
     case 4:
-      if constexpr (!LN) return sp_bwd_tma_kernel<LN, 4, DH, MASK>;
+      if constexpr (!LN) return sp_bwd_tma_kernel<LN, 4, DH, MASK, REGEN>;
       return nullptr;
     default: return nullptr;
   }
 }
 
+// mode: 0 = no dropout, 1 = stored mask, 2 = regenerate the mask
 template <bool LN>
-void (*tma_kernel(int vpt, bool dh, bool mask))(const BwdArgs, const BwdTmaLayout) {
-  if (dh) return mask ? tma_kernel_v<LN, true, true>(vpt) : tma_kernel_v<LN, true, false>(vpt);
-  return mask ? tma_kernel_v<LN, false, true>(vpt) : tma_kernel_v<LN, false, false>(vpt);
+void (*tma_kernel(int vpt, bool dh, int mode))(const BwdArgs, const BwdTmaLayout) {
+  if (dh) {
+    if (mode == 1) return tma_kernel_v<LN, true, true, false>(vpt);
+    if (mode == 2) return tma_kernel_v<LN, true, false, true>(vpt);
+    return tma_kernel_v<LN, true, false, false>(vpt);
+  }
+  if (mode == 1) return tma_kernel_v<LN, false, true, false>(vpt);
+  if (mode == 2) return tma_kernel_v<LN, false, false, true>(vpt);
+  return tma_kernel_v<LN, false, false, false>(vpt);
 }
 
 constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, rounded up
@@ -82,9 +89,10 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
 
 cudaError_t launch_bwd_tma(bool ln, const BwdArgs& a, const BwdTmaPlan& p, dim3 grid,
                            cudaStream_t st) {
-  const bool dh = a.dh != nullptr, mask = a.mask != nullptr;
-  void (*k)(const BwdArgs, const BwdTmaLayout) = ln ? tma_kernel<true>(p.shape.vpt, dh, mask)
-                                                    : tma_kernel<false>(p.shape.vpt, dh, mask);
+  const bool dh = a.dh != nullptr;
+  const int mode = a.mask ? 1 : (a.regen ? 2 : 0);
+  void (*k)(const BwdArgs, const BwdTmaLayout) = ln ? tma_kernel<true>(p.shape.vpt, dh, mode)
+                                                    : tma_kernel<false>(p.shape.vpt, dh, mode);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;

@@ -29,8 +29,9 @@ namespace spf {
 // At most 16 warps (15 consumer + 1 producer), so 128 registers per thread fit
 // every SM sub-partition's register file.  KEEP: dy and xhat stay in registers
 // between the two passes (VPT <= 3); with 4 vectors per thread pass 2 reads
-// them from shared memory again instead.
-template <bool LN, int VPT, bool DH, bool MASK>
+// them from shared memory again instead.  MASK: the keep bits come from the
+// stored mask; REGEN: they are recomputed from the seed (no mask stored).
+template <bool LN, int VPT, bool DH, bool MASK, bool REGEN = false>
 __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
   constexpr bool KEEP = VPT <= 3;
   constexpr int EV = 8;
@@ -222,6 +223,10 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
           if constexpr (DH) wdh = sdh[v];
           uint32_t mk = 0xFFu;
           if constexpr (MASK) mk = ld_mask_shared8(smk + v * EV);
+          if constexpr (REGEN) {
+            const uint64_t g0 = (uint64_t)((a.grow0 + r) * (int64_t)H + (int64_t)v * EV);
+            mk = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
+          }
           uint4 wdy2 = make_uint4(0u, 0u, 0u, 0u), wh2 = make_uint4(0u, 0u, 0u, 0u);
           if constexpr (!KEEP) {
             wdy2 = sdy[v];
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
             else
               dres = f2_mul(r2, t);
             f2_t dsum = f2_mul(dres, sc);
-            if constexpr (MASK) {
+            if constexpr (MASK || REGEN) {
               float sl, sh2;
               f2_split(dsum, sl, sh2);
               dsum = f2(((mk >> (2 * q)) & 1u) ? sl : 0.f, ((mk >> (2 * q + 1)) & 1u) ? sh2 : 0.f);

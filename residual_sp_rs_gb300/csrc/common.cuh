@@ -405,7 +405,7 @@ struct BwdArgs {
   const void* dh;        // [rows, H] or null
   const void* h;         // [rows, H]
   const void* gamma;     // [H]
-  const uint8_t* mask;   // [rows, H] or null (p == 0)
+  const uint8_t* mask;   // [rows, H] or null (p == 0, or regenerate)
   const float* rstd;     // [rows]
   const float* mean;     // [rows] (LayerNorm)
   void* d_res;           // [rows, H]
@@ -417,9 +417,13 @@ struct BwdArgs {
   int32_t H;
   int32_t nvec;
   int32_t tpr;
-  int32_t nparts;        // clusters launched (rows of ws per statistic)
+  int32_t nparts;        // partial rows per statistic
   float scale;           // 1 / (1 - p)
   float Hf;
+  int32_t regen;         // p > 0 without a stored mask: recompute the keep bits
+  uint32_t thr;          // keep threshold (regen)
+  int64_t grow0;         // global row index of local row 0 (regen)
+  PhiloxKeys keys;       // Philox round keys of the seed (regen)
 };
 
 // Shared-memory ring of the TMA-fed forward.

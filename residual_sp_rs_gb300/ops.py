@@ -148,12 +148,15 @@ def hp2sp(inp, out, N, H, T, dtype, stream=None) -> None:
 
 # ---- conveniences that allocate outputs ------------------------------------------
 
-def forward(desc: SpRsDesc, partials, residual, gamma, beta=None, stream=None) -> dict:
+def forward(desc: SpRsDesc, partials, residual, gamma, beta=None, stream=None,
+            store_mask: bool = True) -> dict:
+    """store_mask=False: the mask is not stored (the backward regenerates it)."""
     rows, H = desc.rows, desc.H
     dev, dt = residual.device, residual.dtype
     out = dict(h=torch.empty((rows, H), device=dev, dtype=dt),
                y=torch.empty((rows, H), device=dev, dtype=dt),
-               mask=torch.empty((rows, H), device=dev, dtype=torch.uint8) if desc.p > 0 else None,
+               mask=torch.empty((rows, H), device=dev, dtype=torch.uint8)
+               if desc.p > 0 and store_mask else None,
                rstd=torch.empty(rows, device=dev, dtype=torch.float32),
                mean=torch.empty(rows, device=dev, dtype=torch.float32)
                if desc.norm == SP_LAYERNORM else None)

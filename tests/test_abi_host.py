@@ -94,7 +94,7 @@ def test_fwd_rejects_bad_pointers(spf):
     assert _fwd(spf, d, residual=0) == 1
     assert _fwd(spf, d, beta=0) == 1            # LayerNorm needs beta
     assert _fwd(spf, d, mean=0) == 1            # ... and mean
-    assert _fwd(spf, d, mask=0) == 1            # p > 0 needs the mask
+    assert _fwd(spf, d, mask=0) in (0, 6)       # no stored mask: accepted (6 = no GPU here)
     assert _fwd(spf, d, partials=[FAKE, FAKE + 8]) == 3
     assert _fwd(spf, d, y=FAKE + 2) == 3
     assert _fwd(spf, d, rstd=FAKE + 2) == 3
@@ -115,7 +115,7 @@ def test_bwd_rejects_bad_arguments(spf):
     def call(desc, mask=FAKE, dy=FAKE, ws=FAKE, nbytes=1 << 30):
         return L.sp_rs_dropout_residual_norm_bwd(ctypes.byref(desc), dy, FAKE, FAKE, FAKE, mask, FAKE,
                                                  FAKE, FAKE, FAKE, FAKE, FAKE, ws, nbytes, None)
-    assert call(d, mask=0) == 1
+    assert call(d, mask=0) in (0, 6)            # regenerated mask: accepted (6 = no GPU here)
     assert call(d, dy=0) == 1
     assert call(d, dy=FAKE + 4) == 3
     bad = spf.make_desc(3, 0, 16, 2, 64, "bf16", "rms", 0.1, 1e-6)

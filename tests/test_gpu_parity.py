@@ -320,6 +320,55 @@ def test_bwd_workspace_too_small_is_rejected():
 
 
 # ---------------------------------------------------------------------------
+# mask-free mode: the forward stores no mask, the backward regenerates it
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["pages_rms_bf16", "gpt_ln_bf16", "tiny_rms_f32"])
+def test_mask_free_forward_and_regenerated_backward(name):
+    w = syn.WORKLOADS[name]
+    inp = syn.fwd_inputs(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    d = _desc(w, 0, w.T)
+    rows = d.rows
+    res = inp["residual"].view(rows, w.H)
+    stored = ops.forward(d, inp["partials"], res, inp["gamma"], inp["beta"])
+    free = ops.forward(d, inp["partials"], res, inp["gamma"], inp["beta"], store_mask=False)
+    assert free["mask"] is None
+    for k in ("h", "y", "rstd"):
+        assert torch.equal(stored[k], free[k]), k
+    dy, dh = grads["dy"].view(rows, w.H), grads["dh_out"].view(rows, w.H)
+    with_mask = ops.backward(d, dy, dh, stored["h"], inp["gamma"], stored["mask"], stored["rstd"],
+                             stored["mean"])
+    regen = ops.backward(d, dy, dh, stored["h"], inp["gamma"], None, stored["rstd"], stored["mean"])
+    torch.cuda.synchronize()
+    for k in ("d_res", "d_sum", "dgamma"):   # identical keep decisions: bit-identical results
+        assert torch.equal(with_mask[k], regen[k]), k
+    # and against the oracle (given the oracle's own mask)
+    pr, orc_f, saved, dy_o, dh_o = _bwd_inputs_from_oracle_fwd(w, 0, w.T, inp, grads)
+    out = ops.backward(d, dy_o, dh_o, saved["h"], inp["gamma"], None, saved["rstd"],
+                       saved["mean"] if w.norm == "ln" else None)
+    torch.cuda.synchronize()
+    _check_bwd(w, pr, orc_f["h"], _np(dy_o), _np(dh_o), _np(inp["gamma"]), orc_f["mask"], out)
+
+
+@pytest.mark.parametrize("case", [(3, 21, 1, 776, "bf16", "ln", 0.3), (2, 6, 1, 16384, "bf16", "ln", 0.1)])
+def test_regenerated_mask_register_backward(case):
+    """Shapes that take the register backward (H % 16 != 0; LayerNorm rows too
+    long for the TMA ring)."""
+    T, S, B, H, dt, nm, p = case
+    w = syn.Workload("edge", T, S, B, H, dt, nm, p, 1e-5, 0x0123456789ABCDEF, 0.5, 1.0, 0.5, 1.5, 0.1,
+                     77 + H)
+    inp = syn.fwd_inputs(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    for j in sorted({0, T - 1}):
+        pr, orc_f, saved, dy, dh = _bwd_inputs_from_oracle_fwd(w, j, 1, inp, grads)
+        d = _desc(w, j)
+        out = ops.backward(d, dy, dh, saved["h"], inp["gamma"], None, saved["rstd"], saved["mean"])
+        torch.cuda.synchronize()
+        _check_bwd(w, pr, orc_f["h"], _np(dy), _np(dh), _np(inp["gamma"]), orc_f["mask"], out)
+
+
+# ---------------------------------------------------------------------------
 # layout transforms
 # ---------------------------------------------------------------------------
 
