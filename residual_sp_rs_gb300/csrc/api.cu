@@ -117,12 +117,13 @@ sp_status_t plan_bwd(const Problem& pr, bool has_dh, bool has_mask, BwdPlan* pl)
     if (qe == cudaSuccess)
       qe = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (qe != cudaSuccess) return from_cuda(qe);
+    const int64_t ctas = pr.rows < sms ? (pr.rows > 0 ? pr.rows : 1) : sms;
+    const int64_t rpc = pr.rows > 0 ? (pr.rows + ctas - 1) / ctas : 1;
     BwdTmaPlan probe;
-    if (plan_bwd_tma(pr.H, ln, true, true, optin, &probe)) {
+    if (plan_bwd_tma(pr.H, ln, true, true, optin, rpc, &probe) &&
+        plan_bwd_tma(pr.H, ln, has_dh, has_mask, optin, rpc, &pl->tp)) {
       pl->tma = true;
-      plan_bwd_tma(pr.H, ln, has_dh, has_mask, optin, &pl->tp);
-      const int64_t ctas = pr.rows < sms ? (pr.rows > 0 ? pr.rows : 1) : sms;
-      pl->rows_per_cta = pr.rows > 0 ? (pr.rows + ctas - 1) / ctas : 1;
+      pl->rows_per_cta = rpc;
       pl->ctas = pr.rows > 0 ? (int)((pr.rows + pl->rows_per_cta - 1) / pl->rows_per_cta) : 0;
       pl->nparts = pl->ctas;
       pl->ws_bytes = (size_t)(ctas > 0 ? ctas : 1) * (size_t)pr.H * sizeof(float) * (ln ? 2 : 1);

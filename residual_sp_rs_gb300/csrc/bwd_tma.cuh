@@ -2,15 +2,17 @@
 // memory by the Tensor Memory Accelerator (bulk copies + mbarriers).
 //
 // One persistent CTA per SM owns a contiguous block of token rows.  A
-// producer warp keeps a ring of NST stages full; a stage holds nrg
-// consecutive rows, one per consumer row group, and is filled with one bulk
-// copy per input tensor (dy, h, dh_out, mask) on the stage's "full" mbarrier.
-// Each row group (tpr threads) computes its row of the stage from shared
-// memory; the stage is released on its "empty" mbarrier as soon as every
-// consumer has read it.  The loads of up to NST*nrg rows are in flight at all
+// producer warp keeps a ring of nst stages full; a stage holds rb
+// consecutive rows and is filled with one bulk copy per input tensor (dy, h,
+// dh_out, mask) on the stage's "full" mbarrier.  Rows go to the nrg row
+// groups round robin (row i to group i % nrg); a row group (tpr threads)
+// computes its row from shared memory and releases the row's stage on its
+// "empty" mbarrier.  The loads of up to nst*rb rows are in flight at all
 // times, without holding them in registers, so the HBM pipe stays busy
-// through the row reductions and the stores.  dy and xhat stay in registers
-// between the two passes over a row; gamma sits in shared memory as fp32.
+// through the row reductions and the stores.  With the 512-thread block dy
+// and xhat stay in registers between the two passes over a row; the wider
+// block (fewer registers, for many short rows) reads them from shared memory
+// again.  gamma sits in shared memory as fp32.
 // dgamma/dbeta accumulate in registers per thread-owned column; at the end
 // the row groups' sums go to the idle ring, are added in row-group order and
 // written as one fp32 partial row per CTA, which sp_colsum_kernel reduces in
@@ -26,14 +28,18 @@
 
 namespace spf {
 
-// At most 16 warps (15 consumer + 1 producer), so 128 registers per thread fit
-// every SM sub-partition's register file.  KEEP: dy and xhat stay in registers
-// between the two passes (VPT <= 3); with 4 vectors per thread pass 2 reads
-// them from shared memory again instead.  MASK: the keep bits come from the
-// stored mask; REGEN: they are recomputed from the seed (no mask stored).
-template <bool LN, int VPT, bool DH, bool MASK, bool REGEN = false>
-__global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
-  constexpr bool KEEP = VPT <= 3;
+constexpr int kBwdTmaNarrowBlock = 512;  // the 16-warp block (128 registers)
+
+// NTHR = 512: at most 16 warps (15 consumer + 1 producer), so 128 registers
+// per thread fit every SM sub-partition's register file; a wider block
+// trades registers for warps (768 threads: 80 registers).  KEEP: dy and xhat stay in registers between the
+// two passes (VPT <= 3, 512 threads); otherwise pass 2 reads them from
+// shared memory again.  MASK: the keep bits come from the stored mask;
+// REGEN: they are recomputed from the seed (no mask stored), before the
+// row's data is waited for.
+template <bool LN, int VPT, bool DH, bool MASK, bool REGEN, int NTHR>
+__global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
+  constexpr bool KEEP = VPT <= 3 && NTHR <= 512;
   constexpr int EV = 8;
   constexpr int NS = LN ? 2 : 1;
   __shared__ float red[2 * 32 * 2];
@@ -45,7 +51,7 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   unsigned char* stages = dsm + L.smem_stages;
 
   // kernel parameters used in the hot loop, held in registers
-  const int H = a.H, nvec = a.nvec, tpr = a.tpr, nrg = L.nrg, nst = L.nst;
+  const int H = a.H, nvec = a.nvec, tpr = a.tpr, nrg = L.nrg, nst = L.nst, rb = L.rb;
   const float invH = 1.0f / a.Hf;
   const float scale = a.scale;
   const int nthr_cons = nrg * tpr;
@@ -55,15 +61,16 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_cta;
   const int64_t r1 = min(a.rows, r0 + a.rows_per_cta);
   const int n = r1 > r0 ? (int)(r1 - r0) : 0;
-  const int nstage = (n + nrg - 1) / nrg;  // stages this CTA fills
+  const int nstage = (n + rb - 1) / rb;  // stages this CTA fills
+  const int nslot = nstage * rb;         // row slots, the last stage padded to rb rows
   const size_t rowb = (size_t)H * 2;
 
-  // Producer: fill stage j (rows j*nrg ..) of the ring.
+  // Producer: fill stage j (rows j*rb ..) of the ring.
   auto issue_stage = [&](int j, uint64_t pol) {
     const int s = j % nst;
     unsigned char* st = stages + (size_t)s * L.stage_bytes;
-    const int64_t r = r0 + (int64_t)j * nrg;
-    const int rows = min(nrg, n - j * nrg);
+    const int64_t r = r0 + (int64_t)j * rb;
+    const int rows = min(rb, n - j * rb);
     const uint32_t bb = (uint32_t)(rows * rowb);  // bytes of one bf16 tensor's rows
     mbar_arrive_expect_tx(&full[s], bb * (DH ? 3u : 2u) + (MASK ? (uint32_t)(rows * H) : 0u));
     tma_load_1d(st, reinterpret_cast<const char*>(a.dy) + r * rowb, bb, &full[s], pol);
@@ -81,7 +88,7 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
     s_failed = 0;
     for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], (uint32_t)nthr_cons);  // every consumer releases
+      mbar_init(&empty[s], (uint32_t)(rb * tpr));  // the stage's row groups release
     }
     fence_mbar_init();
     // the first ring's worth of rows goes out before anything else happens
@@ -137,30 +144,60 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
       if constexpr (LN) mu_n = __ldcs(a.mean + r0 + rg);
     }
     const f2_t sc = f2(scale, scale);
-    for (int j = 0; j < nstage; ++j) {
-      const int s = j % nst;
+    // row slot i, its stage j = i / rb, the stage's row ri = i % rb, ring
+    // slot s = j % nst and phase parity (j / nst) & 1.  The 512-thread block
+    // always has rb == nrg (iteration jj is stage jj, ri = rg), which keeps
+    // its register budget; the wide block keeps them incrementally.
+    constexpr bool kStageMajor = NTHR <= kBwdTmaNarrowBlock;
+    int ri = rg % rb, s = (rg / rb) % nst, par = ((rg / rb) / nst) & 1;
+    for (int i = rg, jj = 0; i < nslot; i += nrg, ++jj) {
+      if constexpr (kStageMajor) {
+        ri = rg;
+        s = jj % nst;
+        par = (jj / nst) & 1;
+      } else if (i != rg) {
+        ri += nrg;
+        while (ri >= rb) {
+          ri -= rb;
+          if (++s == nst) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
+      uint32_t keep[REGEN ? VPT : 1];
+      if constexpr (REGEN) {  // depends only on the element index: before the wait
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          const int v = lr + k * tpr;
+          keep[k] = 0xFFu;
+          if (i < n && (k < VPT - 1 || last_in)) {
+            const uint64_t g0 = (uint64_t)((a.grow0 + r0 + i) * (int64_t)H + (int64_t)v * EV);
+            keep[k] = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
+          }
+        }
+      }
       // the whole row group agrees on the outcome of the wait before any of
       // it enters the row reduction's named barrier
       // (one-warp row groups vote; wider ones use their named barrier, id <= 8)
-      const bool landed = mbar_wait(&full[s], (uint32_t)((j / nst) & 1));
+      const bool landed = mbar_wait(&full[s], (uint32_t)par);
       const bool all_landed =
           tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
       if (!all_landed) {
         ok = false;
         break;
       }
-      const int i = j * nrg + rg;  // this row group's row of the stage
-      if (i >= n) {                // last stage short of rows: just release it
+      if (i >= n) {  // padding of the last stage: just release it
         mbar_arrive(&empty[s]);
         continue;
       }
       const unsigned char* st = stages + (size_t)s * L.stage_bytes;
-      const size_t rofs = (size_t)rg * rowb;  // this row inside each tensor's block
+      const int64_t r = r0 + i;
+      const size_t rofs = (size_t)ri * rowb;  // this row inside each tensor's block
       const uint4* sdy = reinterpret_cast<const uint4*>(st + rofs);
       const uint4* sh = reinterpret_cast<const uint4*>(st + L.off_h + rofs);
       const uint4* sdh = reinterpret_cast<const uint4*>(st + L.off_dh + rofs);
-      const uint8_t* smk = st + L.off_mask + (size_t)rg * H;
-      const int64_t r = r0 + i;
+      const uint8_t* smk = st + L.off_mask + (size_t)ri * H;
       const float rstd = rstd_n;
       const float mu = mu_n;
       if (i + nrg < n) {
@@ -223,10 +260,7 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
           if constexpr (DH) wdh = sdh[v];
           uint32_t mk = 0xFFu;
           if constexpr (MASK) mk = ld_mask_shared8(smk + v * EV);
-          if constexpr (REGEN) {
-            const uint64_t g0 = (uint64_t)((a.grow0 + r) * (int64_t)H + (int64_t)v * EV);
-            mk = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
-          }
+          if constexpr (REGEN) mk = keep[k];
           uint4 wdy2 = make_uint4(0u, 0u, 0u, 0u), wh2 = make_uint4(0u, 0u, 0u, 0u);
           if constexpr (!KEEP) {
             wdy2 = sdy[v];
@@ -276,23 +310,29 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   __syncthreads();  // every stage consumed and landed: the ring is free
 
   // ---- dgamma/dbeta: row groups' column sums into the ring, added in order ---
-  float* part = reinterpret_cast<float*>(stages);  // [nrg][NS][H]
+  // The ring holds them as [nrg][NS][EV][pitch], pitch = nvec + 4: element e
+  // of vector v (column v*EV + e) at e*pitch + v.  A warp's stores (fixed e,
+  // consecutive v) hit consecutive banks, and so do the reads of 32
+  // consecutive columns (the 8 elements of a vector 4 banks apart).
+  const int pitch = nvec + 4;
+  const size_t plane = (size_t)EV * pitch;  // floats per row group and statistic
+  float* part = reinterpret_cast<float*>(stages);
   if (!producer) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lr + k * tpr;
       if (v < nvec) {
-        float* dst = part + (size_t)rg * NS * H + v * EV;
+        float* dst = part + (size_t)rg * NS * plane + v;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float lo, hi;
           f2_split(dg[k][q], lo, hi);
-          dst[2 * q] = lo;
-          dst[2 * q + 1] = hi;
+          dst[(2 * q) * pitch] = lo;
+          dst[(2 * q + 1) * pitch] = hi;
           if constexpr (LN) {
             f2_split(db[k][q], lo, hi);
-            dst[H + 2 * q] = lo;
-            dst[H + 2 * q + 1] = hi;
+            dst[plane + (2 * q) * pitch] = lo;
+            dst[plane + (2 * q + 1) * pitch] = hi;
           }
         }
       }
@@ -301,12 +341,14 @@ __global__ void __launch_bounds__(512, 1) sp_bwd_tma_kernel(const BwdArgs a, con
   __syncthreads();
   // a CTA whose wait timed out poisons its partial so dgamma/dbeta are NaN
   const bool failed = s_failed != 0;
-  for (int c = threadIdx.x; c < NS * H; c += blockDim.x) {
-    float acc = part[c];
-    for (int g = 1; g < nrg; ++g) acc += part[(size_t)g * NS * H + c];
-    const int st = c / H;
-    __stcg(a.ws + ((int64_t)st * a.nparts + blockIdx.x) * H + (c - st * H),
-           failed ? __int_as_float(0x7FC00000) : acc);
+  for (int st = 0; st < NS; ++st) {
+    float* dst = a.ws + ((int64_t)st * a.nparts + blockIdx.x) * H;
+    for (int c = threadIdx.x; c < H; c += blockDim.x) {
+      const size_t x = (size_t)(c & (EV - 1)) * pitch + (c / EV);
+      float acc = part[st * plane + x];
+      for (int g = 1; g < nrg; ++g) acc += part[((size_t)g * NS + st) * plane + x];
+      __stcg(dst + c, failed ? __int_as_float(0x7FC00000) : acc);
+    }
   }
 }
 

@@ -429,9 +429,10 @@ struct BwdArgs {
 // Shared-memory ring of the TMA-fed forward.
 struct FwdTmaLayout {
   int32_t nst;           // stages in the ring
-  int32_t nrg;           // consumer row groups (rows per stage)
+  int32_t nrg;           // consumer row groups
+  int32_t rb;            // rows per stage
   uint32_t stage_bytes;  // bytes of one stage
-  uint32_t blk;          // bytes of one tensor's rows in a stage (nrg * H * 2)
+  uint32_t blk;          // bytes of one tensor's rows in a stage (rb * H * 2)
   uint32_t smem_stages;  // offset of stage 0 in dynamic shared memory
   int64_t rows_per_cta;
 };
@@ -440,6 +441,7 @@ struct FwdTmaLayout {
 struct BwdTmaLayout {
   int32_t nst;          // stages in the ring
   int32_t nrg;          // consumer row groups
+  int32_t rb;           // rows per stage
   uint32_t stage_bytes; // bytes of one stage
   uint32_t off_h, off_dh, off_mask;  // offsets inside a stage (dy at 0)
   uint32_t smem_stages; // offset of stage 0 in dynamic shared memory

@@ -2,14 +2,22 @@
 // memory by the Tensor Memory Accelerator (bf16).
 //
 // One persistent CTA per SM owns a contiguous block of token rows.  A
-// producer warp keeps a ring of NST stages full; a stage holds nrg
-// consecutive rows (one per consumer row group) of each of the T partials
-// and of the residual, each filled with one bulk copy on the stage's "full"
-// mbarrier.  Consumer row groups reduce, mask, add and normalise their row
-// from shared memory and release the stage on its "empty" mbarrier, so the
-// arithmetic of one stage overlaps the loads of the next ones.  gamma/beta
-// are kept in shared memory as fp32.  Used when a stage of rows fits twice in
-// shared memory; longer rows (T*H large) take the register-resident kernel.
+// producer warp keeps a ring of nst stages full; a stage holds rb
+// consecutive rows of each of the T partials and of the residual, each
+// filled with one bulk copy on the stage's "full" mbarrier.  Rows go to the
+// nrg consumer row groups round robin (row i to group i % nrg); a group
+// reduces, masks, adds and normalises its row from shared memory and
+// releases the row's stage on its "empty" mbarrier, so the arithmetic of
+// one row overlaps the loads of the next ones.  Small stages (down to one
+// row) let the first rows start as soon as they land.  gamma/beta are kept
+// in shared memory as fp32.  NTHR is the block size the registers are
+// budgeted for: 544 (16 consumer warps + producer, up to 120 registers) or
+// 1024 (64 registers) for the many short rows of small T.
+//
+// The mask depends only on the element index, so a thread draws (and
+// stores) its row's keep bits before it waits for the row's data: the
+// Philox arithmetic overlaps the loads.  Used when two stages fit in shared
+// memory; longer rows (T*H large) take the register-resident kernel.
 //
 // If a wait times out, the row group stops and writes NaN into the rstd of
 // the rows it did not finish, so the failure is visible in the outputs.
@@ -98,9 +106,25 @@ __device__ __forceinline__ void residual_vec8_drop(const f2_t (&acc)[4], const f
 
 // FAST: p > 0 with 1/(1-p) not dyadic (the common case) -- no tie rule, no
 // runtime mode branches in the element loop.  Otherwise GENERIC.
-template <int T, bool LN, int VPT, bool FAST>
-__global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, const FwdTmaLayout L) {
+template <int VPT, bool PACK>
+struct HRow;
+template <int VPT>
+struct HRow<VPT, false> {
+  f2_t v[VPT][4];
+  __device__ __forceinline__ void set(int k, int q, uint32_t, f2_t f) { v[k][q] = f; }
+  __device__ __forceinline__ f2_t get(int k, int q) const { return v[k][q]; }
+};
+template <int VPT>
+struct HRow<VPT, true> {
+  uint32_t w[VPT][4];
+  __device__ __forceinline__ void set(int k, int q, uint32_t b, f2_t) { w[k][q] = b; }
+  __device__ __forceinline__ f2_t get(int k, int q) const { return bf2_to_f2(w[k][q]); }
+};
+
+template <int T, bool LN, int VPT, bool FAST, int NTHR>
+__global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, const FwdTmaLayout L) {
   constexpr int EV = 8;
+  constexpr bool kPackH = NTHR > 544;
   __shared__ float red[2 * 32 * 2];
   extern __shared__ __align__(16) unsigned char dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
@@ -111,21 +135,22 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
   const int H = a.H, nvec = a.nvec, tpr = a.tpr;
   const float invH = 1.0f / a.Hf;
   const int nthr_cons = L.nrg * tpr;
-  const bool producer = threadIdx.x >= nthr_cons;
+  const bool producer = (int)threadIdx.x >= nthr_cons;
   const int rg = producer ? L.nrg : (int)threadIdx.x / tpr;
   const int lr = (int)threadIdx.x - rg * tpr;
   const int64_t r0 = (int64_t)blockIdx.x * L.rows_per_cta;
   const int64_t r1 = min(a.rows, r0 + L.rows_per_cta);
   const int n = r1 > r0 ? (int)(r1 - r0) : 0;
-  const int nstage = (n + L.nrg - 1) / L.nrg;
+  const int nstage = (n + L.rb - 1) / L.rb;
+  const int nslot = nstage * L.rb;  // row slots, the last stage padded to rb rows
   const size_t rowb = (size_t)H * 2;
   const uint64_t pol = policy_evict_first();
 
   auto issue_stage = [&](int j) {
     const int s = j % L.nst;
     unsigned char* st = stages + (size_t)s * L.stage_bytes;
-    const int64_t r = r0 + (int64_t)j * L.nrg;  // local row of the stage's first row
-    const int rows = min(L.nrg, n - j * L.nrg);
+    const int64_t r = r0 + (int64_t)j * L.rb;  // local row of the stage's first row
+    const int rows = min(L.rb, n - j * L.rb);
     const uint32_t bb = (uint32_t)(rows * rowb);
     mbar_arrive_expect_tx(&full[s], bb * (uint32_t)(T + 1));
 #pragma unroll
@@ -143,7 +168,7 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
   if (lead) {
     for (int s = 0; s < L.nst; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], (uint32_t)nthr_cons);
+      mbar_init(&empty[s], (uint32_t)(L.rb * tpr));
     }
     fence_mbar_init();
     for (; issued < min(nstage, L.nst); ++issued) issue_stage(issued);
@@ -180,30 +205,56 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
   const f2_t shi = f2(a.scale, a.scale), slo = f2(a.scale_lo, a.scale_lo);
   const bool dropout = a.dropout != 0, nontie = a.dropout && !a.dyadic_scale;
   const bool last_in = lr + (VPT - 1) * tpr < nvec;  // the last vector slot may fall outside
-  for (int j = 0; j < nstage; ++j) {
-    const int s = j % L.nst;
-    const bool landed = mbar_wait(&full[s], (uint32_t)((j / L.nst) & 1));
+  // row slot i, its stage j = i / rb, the stage's row ri = i % rb, ring slot
+  // s = j % nst and phase parity (j / nst) & 1, kept incrementally
+  int ri = rg % L.rb, s = (rg / L.rb) % L.nst, par = ((rg / L.rb) / L.nst) & 1;
+  for (int i = rg; i < nslot; i += L.nrg) {
+    if (i != rg) {
+      ri += L.nrg;
+      while (ri >= L.rb) {
+        ri -= L.rb;
+        if (++s == L.nst) {
+          s = 0;
+          par ^= 1;
+        }
+      }
+    }
+    const int64_t r = r0 + i;
+    const int64_t grow = a.grow0 + r;
+
+    // ---- draw (and store) the row's mask before waiting for its data
+    uint32_t keep[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      keep[k] = 0xFFu;
+      const int v = lr + k * tpr;
+      if ((FAST || dropout) && i < n && (k < VPT - 1 || last_in)) {
+        const uint64_t g0 = (uint64_t)(grow * H + (int64_t)v * EV);
+        keep[k] = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
+        if (a.mask) st_mask<EV>(a.mask + r * (int64_t)H + v * EV, keep[k]);
+      }
+    }
+
+    const bool landed = mbar_wait(&full[s], (uint32_t)par);
     const bool all_landed =
         tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
     if (!all_landed) {  // give up: mark this row group's remaining rows
-      for (int i = j * L.nrg + rg; i < n; i += L.nrg)
-        if (lr == 0) a.rstd[r0 + i] = __int_as_float(0x7FC00000);
+      for (int k = i; k < n; k += L.nrg)
+        if (lr == 0) a.rstd[r0 + k] = __int_as_float(0x7FC00000);
       return;
     }
-    const int i = j * L.nrg + rg;
-    if (i >= n) {
+    if (i >= n) {  // padding of the last stage
       mbar_arrive(&empty[s]);
       continue;
     }
-    const unsigned char* st = stages + (size_t)s * L.stage_bytes + (size_t)rg * rowb;
-    const int64_t r = r0 + i;
-    const int64_t grow = a.grow0 + r;
+    const unsigned char* st = stages + (size_t)s * L.stage_bytes + (size_t)ri * rowb;
     __nv_bfloat16* h_row = reinterpret_cast<__nv_bfloat16*>(a.h) + r * (int64_t)H;
     __nv_bfloat16* y_row = reinterpret_cast<__nv_bfloat16*>(a.y) + r * (int64_t)H;
-    uint8_t* m_row = a.mask ? a.mask + r * (int64_t)H : nullptr;
 
-    // ---- reduce, mask, dropout, residual add; store h and the mask --------
-    f2_t hf[VPT][4];
+    // ---- reduce, dropout, residual add; store h ----------------------------
+    // h stays in registers for the norm: as fp32 pairs, or (1024-thread
+    // block, 64 registers) as the stored bf16 pairs, unpacked again per use
+    HRow<VPT, kPackH> hf;
     f2_t s2 = f2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -213,10 +264,7 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
 #pragma unroll
         for (int t = 0; t < T; ++t) pw[t] = reinterpret_cast<const uint4*>(st + (size_t)t * L.blk)[v];
         const uint4 rw = reinterpret_cast<const uint4*>(st + (size_t)T * L.blk)[v];
-        const uint64_t g0 = (uint64_t)(grow * H + (int64_t)v * EV);
-        uint32_t keep = 0xFFu;
-        if (FAST || dropout)
-          keep = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
+        const uint32_t kb = keep[k];
         uint32_t hw[4];
         if constexpr (FAST) {
           f2_t acc[4], res[4];
@@ -228,14 +276,15 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
               acc[q] = f2_add(acc[q], bf2_to_f2(reinterpret_cast<const uint32_t*>(&pw[t])[q]));
             float al, ah;
             f2_split(acc[q], al, ah);
-            acc[q] = f2(((keep >> (2 * q)) & 1u) ? al : 0.f, ((keep >> (2 * q + 1)) & 1u) ? ah : 0.f);
+            acc[q] = f2(((kb >> (2 * q)) & 1u) ? al : 0.f, ((kb >> (2 * q + 1)) & 1u) ? ah : 0.f);
             res[q] = bf2_to_f2(reinterpret_cast<const uint32_t*>(&rw)[q]);
           }
           residual_vec8_drop(acc, res, shi, slo, hw);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            hf[k][q] = bf2_to_f2(hw[q]);
-            s2 = LN ? f2_add(s2, hf[k][q]) : f2_fma(hf[k][q], hf[k][q], s2);
+            const f2_t hq = bf2_to_f2(hw[q]);
+            hf.set(k, q, hw[q], hq);
+            s2 = LN ? f2_add(s2, hq) : f2_fma(hq, hq, s2);
           }
         } else {
 #pragma unroll
@@ -248,15 +297,15 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
           if (dropout) {
             float al, ah;
             f2_split(acc, al, ah);
-            acc = f2(((keep >> (2 * q)) & 1u) ? al : 0.f, ((keep >> (2 * q + 1)) & 1u) ? ah : 0.f);
+            acc = f2(((kb >> (2 * q)) & 1u) ? al : 0.f, ((kb >> (2 * q + 1)) & 1u) ? ah : 0.f);
           }
           hw[q] = nontie ? residual_bf2_drop(res, acc, shi, slo) : residual_bf2(res, acc, shi, slo);
-          hf[k][q] = bf2_to_f2(hw[q]);
-          s2 = LN ? f2_add(s2, hf[k][q]) : f2_fma(hf[k][q], hf[k][q], s2);
+          const f2_t hq = bf2_to_f2(hw[q]);
+          hf.set(k, q, hw[q], hq);
+          s2 = LN ? f2_add(s2, hq) : f2_fma(hq, hq, s2);
         }
         }
         st_stream(h_row + v * EV, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-        if (m_row) st_mask<EV>(m_row + v * EV, keep);
       }
     }
     mbar_arrive(&empty[s]);  // the stage is no longer read
@@ -279,7 +328,7 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
         if (k < VPT - 1 || last_in) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const f2_t dd = f2_sub(hf[k][q], mu2);
+            const f2_t dd = f2_sub(hf.get(k, q), mu2);
             q2 = f2_fma(dd, dd, q2);
           }
         }
@@ -310,12 +359,12 @@ __global__ void __launch_bounds__(544, 1) sp_fwd_tma_kernel(const FwdArgs a, con
           const f2_t ga = f2(g4.x, g4.y), gb = f2(g4.z, g4.w);
           if constexpr (LN) {
             const float4 b4 = reinterpret_cast<const float4*>(sgb + H + v * EV)[q2];
-            yw[2 * q2] = f2_to_bf2(f2_fma(ga, f2_mul(f2_sub(hf[k][2 * q2], mu2), r2), f2(b4.x, b4.y)));
+            yw[2 * q2] = f2_to_bf2(f2_fma(ga, f2_mul(f2_sub(hf.get(k, 2 * q2), mu2), r2), f2(b4.x, b4.y)));
             yw[2 * q2 + 1] =
-                f2_to_bf2(f2_fma(gb, f2_mul(f2_sub(hf[k][2 * q2 + 1], mu2), r2), f2(b4.z, b4.w)));
+                f2_to_bf2(f2_fma(gb, f2_mul(f2_sub(hf.get(k, 2 * q2 + 1), mu2), r2), f2(b4.z, b4.w)));
           } else {
-            yw[2 * q2] = f2_to_bf2(f2_mul(ga, f2_mul(hf[k][2 * q2], r2)));
-            yw[2 * q2 + 1] = f2_to_bf2(f2_mul(gb, f2_mul(hf[k][2 * q2 + 1], r2)));
+            yw[2 * q2] = f2_to_bf2(f2_mul(ga, f2_mul(hf.get(k, 2 * q2), r2)));
+            yw[2 * q2 + 1] = f2_to_bf2(f2_mul(gb, f2_mul(hf.get(k, 2 * q2 + 1), r2)));
           }
         }
         st_stream(y_row + v * EV, make_uint4(yw[0], yw[1], yw[2], yw[3]));

@@ -1,5 +1,6 @@
 // fwd_tma_inst.cuh -- instances of the TMA-fed forward for one norm over
-// T = 1..8, VPT = 1..3 and the fast / generic rounding mode.
+// T = 1..8, VPT = 1..3, the fast / generic rounding mode and the two block
+// sizes (the 1024-thread one only for T <= 4).
 #pragma once
 
 #include "fwd_tma.cuh"
@@ -7,19 +8,29 @@
 
 namespace spf {
 
-template <bool LN, int T, bool FAST>
+template <bool LN, int T, bool FAST, int NTHR>
 inline void (*fwd_tma_kernel_for_vpt(int vpt))(const FwdArgs, const FwdTmaLayout) {
   switch (vpt) {
-    case 1: return sp_fwd_tma_kernel<T, LN, 1, FAST>;
-    case 2: return sp_fwd_tma_kernel<T, LN, 2, FAST>;
-    case 3: return sp_fwd_tma_kernel<T, LN, 3, FAST>;
+    case 1: return sp_fwd_tma_kernel<T, LN, 1, FAST, NTHR>;
+    case 2: return sp_fwd_tma_kernel<T, LN, 2, FAST, NTHR>;
+    case 3: return sp_fwd_tma_kernel<T, LN, 3, FAST, NTHR>;
     default: return nullptr;
   }
 }
 
+template <bool LN, int T, int NTHR>
+inline void (*fwd_tma_kernel_for_mode(int vpt, bool fast))(const FwdArgs, const FwdTmaLayout) {
+  return fast ? fwd_tma_kernel_for_vpt<LN, T, true, NTHR>(vpt)
+              : fwd_tma_kernel_for_vpt<LN, T, false, NTHR>(vpt);
+}
+
 template <bool LN, int T>
-inline void (*fwd_tma_kernel_for(int vpt, bool fast))(const FwdArgs, const FwdTmaLayout) {
-  return fast ? fwd_tma_kernel_for_vpt<LN, T, true>(vpt) : fwd_tma_kernel_for_vpt<LN, T, false>(vpt);
+inline void (*fwd_tma_kernel_for(int vpt, bool fast, int nthr))(const FwdArgs, const FwdTmaLayout) {
+  if (nthr == kFwdTmaWide) {
+    if constexpr (T <= kFwdTmaWideMaxT) return fwd_tma_kernel_for_mode<LN, T, kFwdTmaWide>(vpt, fast);
+    return nullptr;
+  }
+  return fwd_tma_kernel_for_mode<LN, T, kFwdTmaDeep>(vpt, fast);
 }
 
 template <bool LN>
@@ -28,14 +39,14 @@ cudaError_t launch_fwd_tma_impl(const FwdArgs& a, int T, const FwdTmaPlan& p, di
   void (*k)(const FwdArgs, const FwdTmaLayout) = nullptr;
   const bool fast = a.dropout && !a.dyadic_scale;
   switch (T) {
-    case 1: k = fwd_tma_kernel_for<LN, 1>(p.shape.vpt, fast); break;
-    case 2: k = fwd_tma_kernel_for<LN, 2>(p.shape.vpt, fast); break;
-    case 3: k = fwd_tma_kernel_for<LN, 3>(p.shape.vpt, fast); break;
-    case 4: k = fwd_tma_kernel_for<LN, 4>(p.shape.vpt, fast); break;
-    case 5: k = fwd_tma_kernel_for<LN, 5>(p.shape.vpt, fast); break;
-    case 6: k = fwd_tma_kernel_for<LN, 6>(p.shape.vpt, fast); break;
-    case 7: k = fwd_tma_kernel_for<LN, 7>(p.shape.vpt, fast); break;
-    case 8: k = fwd_tma_kernel_for<LN, 8>(p.shape.vpt, fast); break;
+    case 1: k = fwd_tma_kernel_for<LN, 1>(p.shape.vpt, fast, p.nthr); break;
+    case 2: k = fwd_tma_kernel_for<LN, 2>(p.shape.vpt, fast, p.nthr); break;
+    case 3: k = fwd_tma_kernel_for<LN, 3>(p.shape.vpt, fast, p.nthr); break;
+    case 4: k = fwd_tma_kernel_for<LN, 4>(p.shape.vpt, fast, p.nthr); break;
+    case 5: k = fwd_tma_kernel_for<LN, 5>(p.shape.vpt, fast, p.nthr); break;
+    case 6: k = fwd_tma_kernel_for<LN, 6>(p.shape.vpt, fast, p.nthr); break;
+    case 7: k = fwd_tma_kernel_for<LN, 7>(p.shape.vpt, fast, p.nthr); break;
+    case 8: k = fwd_tma_kernel_for<LN, 8>(p.shape.vpt, fast, p.nthr); break;
     default: break;
   }
   if (!k) return cudaErrorInvalidValue;

@@ -3,58 +3,78 @@
 
 namespace spf {
 
+#ifndef SPF_FWD_TMA_MIN_COPY
+#define SPF_FWD_TMA_MIN_COPY 8192
+#endif
+#ifndef SPF_FWD_TMA_MAX_BLOCK
+#define SPF_FWD_TMA_MAX_BLOCK 1024
+#endif
+
 namespace {
 constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, rounded up
-constexpr int kMaxConsumers = 512;
+constexpr int kMaxStages = 48;
+// smallest bulk copy worth issuing: a stage takes enough rows that each of
+// its T+1 copies moves at least this many bytes (up to one row per group)
+constexpr size_t kMinCopy = SPF_FWD_TMA_MIN_COPY;
+constexpr int kMaxBlock = SPF_FWD_TMA_MAX_BLOCK;
+
+int ring_stages(size_t stage, size_t gb, size_t budget) {
+  for (int cand = kMaxStages; cand >= 2; --cand) {
+    const size_t bars = 16 * (((size_t)2 * cand * 8 + 15) / 16);
+    if (bars + gb + (size_t)cand * stage <= budget) return cand;
+  }
+  return 0;
+}
 }  // namespace
 
-// Picks the row-group width (<= 3 vectors per thread) and rows per stage that
-// give the most consumer threads while at least two stages fit in shared
-// memory next to gamma/beta; false when no such ring exists (long rows).
+// Picks the narrowest row group (<= 3 vectors per thread), as many row groups
+// as the block size allows but no more than the rows a CTA owns, and stages
+// of rb rows (copies of at least kMinCopy bytes where the ring allows), as
+// many as fit in shared memory next to gamma/beta (at least two); false when
+// two one-row stages do not fit (long rows).  T <= 4 takes the 1024-thread
+// block (more rows in flight per SM); larger T the 544-thread one, which
+// leaves each thread more registers.
 bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms, FwdTmaPlan* p) {
   const int nvec = (int)(H / 8);
   const size_t rowb = (size_t)H * 2;
   const size_t gb = (size_t)H * 4 * (ln ? 2 : 1);
   const size_t budget = (size_t)max_smem - kStaticSmem;
-  bool found = false;
-  int best_threads = 0;
-  for (int tpr = 32; tpr <= kMaxConsumers; tpr *= 2) {
+  const int64_t ctas = rows < sms ? (rows > 0 ? rows : 1) : sms;
+  const int64_t rows_per_cta = rows > 0 ? (rows + ctas - 1) / ctas : 1;
+  const bool wide = T <= kFwdTmaWideMaxT && kMaxBlock >= kFwdTmaWide;
+  const int cons_warps = (wide ? kFwdTmaWide : kFwdTmaDeep) / 32 - 1;
+  for (int tpr = 32; tpr / 32 <= cons_warps; tpr *= 2) {
     const int vpt = (nvec + tpr - 1) / tpr;
     if (vpt > 3) continue;
-    for (int nrg = kMaxConsumers / tpr; nrg >= 1; nrg /= 2) {
-      if (tpr > 32 && nrg > 15) continue;  // named barriers 1..nrg
-      const size_t blk = (size_t)nrg * rowb;
-      const size_t stage = blk * (size_t)(T + 1);
-      int nst = 0;
-      for (int cand = 4; cand >= 2; --cand) {
-        const size_t bars = 16 * (((size_t)2 * cand * 8 + 15) / 16);
-        if (bars + gb + (size_t)cand * stage <= budget) {
-          nst = cand;
-          break;
-        }
-      }
-      if (nst < 2) continue;
-      if (nrg * tpr > best_threads) {
-        best_threads = nrg * tpr;
-        found = true;
-        FwdTmaLayout L = {};
-        L.nst = nst;
-        L.nrg = nrg;
-        L.stage_bytes = (uint32_t)stage;
-        L.blk = (uint32_t)blk;
-        L.smem_stages = (uint32_t)(16 * (((size_t)2 * nst * 8 + 15) / 16) + gb);
-        const int64_t ctas = rows < sms ? (rows > 0 ? rows : 1) : sms;
-        L.rows_per_cta = rows > 0 ? (rows + ctas - 1) / ctas : 1;
-        p->layout = L;
-        p->shape.tpr = tpr;
-        p->shape.vpt = vpt;
-        p->shape.block = nrg * tpr + 32;
-        p->smem = L.smem_stages + (size_t)nst * stage;
-      }
-      break;  // the largest fitting nrg for this width
+    int nrg = cons_warps / (tpr / 32);
+    if (tpr > 32 && nrg > 15) nrg = 15;  // named barriers 1..nrg
+    if ((int64_t)nrg > rows_per_cta) nrg = (int)rows_per_cta;
+    int rb = (int)((kMinCopy + rowb - 1) / rowb);
+    rb = rb < 1 ? 1 : (rb > nrg ? nrg : rb);
+    int nst = 0;
+    for (; rb >= 1; --rb) {
+      nst = ring_stages((size_t)rb * (T + 1) * rowb, gb, budget);
+      if (nst >= 2) break;
     }
+    if (rb < 1) return false;  // wider row groups do not shorten the rows
+    const size_t stage = (size_t)rb * (T + 1) * rowb;
+    FwdTmaLayout L = {};
+    L.nst = nst;
+    L.nrg = nrg;
+    L.rb = rb;
+    L.stage_bytes = (uint32_t)stage;
+    L.blk = (uint32_t)(rb * rowb);
+    L.smem_stages = (uint32_t)(16 * (((size_t)2 * nst * 8 + 15) / 16) + gb);
+    L.rows_per_cta = rows_per_cta;
+    p->layout = L;
+    p->shape.tpr = tpr;
+    p->shape.vpt = vpt;
+    p->shape.block = nrg * tpr + 32;
+    p->nthr = wide ? kFwdTmaWide : kFwdTmaDeep;
+    p->smem = L.smem_stages + (size_t)nst * stage;
+    return true;
   }
-  return found;
+  return false;
 }
 
 }  // namespace spf

@@ -54,18 +54,37 @@ cudaError_t launch_colsum(const float* ws, int nparts, int H, bool ln, float* dg
                           float* dbeta, cudaStream_t st);
 
 // TMA-fed backward (bf16, H % 16 == 0): shared-memory ring layout and shape.
+// Block sizes the TMA backward is compiled for: 15 consumer warps + producer
+// (128 registers), or 23 + producer (80 registers, up to 3 vectors a thread).
+#ifndef SPF_BWD_TMA_WIDE
+#define SPF_BWD_TMA_WIDE 768
+#endif
+constexpr int kBwdTmaNarrow = 512;
+constexpr int kBwdTmaWide = SPF_BWD_TMA_WIDE;
+
 struct BwdTmaPlan {
   RowShape shape;
   size_t smem;
+  int nthr;  // kBwdTmaNarrow or kBwdTmaWide
   BwdTmaLayout layout;
 };
-bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, BwdTmaPlan* p);
+bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, int64_t rows_per_cta,
+                  BwdTmaPlan* p);
 cudaError_t launch_bwd_tma(bool ln, const BwdArgs& a, const BwdTmaPlan& p, dim3 grid, cudaStream_t st);
+cudaError_t launch_bwd_tma_rms(const BwdArgs& a, const BwdTmaPlan& p, dim3 grid, cudaStream_t st);
+cudaError_t launch_bwd_tma_ln(const BwdArgs& a, const BwdTmaPlan& p, dim3 grid, cudaStream_t st);
 
 // TMA-fed forward (bf16, rows short enough for a two-stage ring).
+// Block sizes the TMA forward is compiled for: 16 consumer warps + producer
+// (registers for T up to 8), or 31 + producer (64 registers, T <= 4).
+constexpr int kFwdTmaDeep = 544;
+constexpr int kFwdTmaWide = 1024;
+constexpr int kFwdTmaWideMaxT = 4;
+
 struct FwdTmaPlan {
   RowShape shape;
   size_t smem;
+  int nthr;  // kFwdTmaDeep or kFwdTmaWide
   FwdTmaLayout layout;
 };
 bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms, FwdTmaPlan* p);

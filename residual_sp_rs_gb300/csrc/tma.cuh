@@ -1,15 +1,19 @@
 // tma.cuh -- bulk asynchronous copies (TMA, 1-D) and mbarriers, inline PTX.
 //
-// Every wait is bounded: after kWaitLimit polls (with a short sleep between
-// them) the waiter gives up and reports false, so a copy that never lands
-// cannot hang the GPU; the caller then marks its results invalid.
+// Every wait is bounded: after about kWaitNs (or kWaitLimit polls) the
+// waiter gives up and reports false, so a copy that never lands cannot hang
+// the GPU; the caller then marks its results invalid.  A waiting thread is
+// suspended by the hardware between polls, so waiters take no issue slots
+// from the warps that still work.
 #pragma once
 
 #include <stdint.h>
 
 namespace spf {
 
-constexpr uint32_t kWaitLimit = 1u << 22;  // ~ 0.1-1 s of polling
+constexpr uint32_t kWaitLimit = 1u << 22;       // polls
+constexpr uint64_t kWaitNs = 2000000000ull;      // 2 s
+constexpr uint32_t kSuspendNs = 100000;          // longest suspension per poll
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -47,12 +51,45 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0u;
 }
 
+// As mbar_try_wait, letting the hardware suspend the thread for up to `ns`
+// nanoseconds while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0u;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+#ifndef SPF_WAIT_MODE
+#define SPF_WAIT_MODE 1
+#endif
+
 // Wait for the phase with the given parity to complete; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+#if SPF_WAIT_MODE == 1
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+#else
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i > 64) __nanosleep(64);
   }
+#endif
   return false;
 }
 
