@@ -196,9 +196,9 @@ __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
 // Second pass: dgamma[c] (and dbeta[c]) = the sum over partial rows
 // p = 0..nparts-1.  blockDim (32, 32): x picks a float4 column of a 32-column
 // group, y a stride class of partial rows (p = y, y+32, ...).  Each thread
-// issues all its loads (up to 8 per round) before adding, then warp 0 adds the
-// 32 stride sums in y order.  The order is fixed, so the result is
-// bit-identical from run to run.
+// issues all its loads (up to 8 per round) before adding, then the 32 stride
+// sums are added pairwise (y + 16, 8, 4, 2, 1).  The order is fixed, so the
+// result is bit-identical from run to run.
 __global__ void __launch_bounds__(1024) sp_colsum_kernel(const float* ws, int nparts, int H,
                                                          float* dgamma, float* dbeta) {
   __shared__ float4 part[32][32];
@@ -228,19 +228,21 @@ __global__ void __launch_bounds__(1024) sp_colsum_kernel(const float* ws, int np
       }
     }
   }
+  // the 32 stride sums of a column, added pairwise in a fixed tree
   part[threadIdx.y][threadIdx.x] = acc;
-  __syncthreads();
-  if (threadIdx.y == 0 && c4 < n4) {
-    float4 s = part[0][threadIdx.x];
-    for (int q = 1; q < 32; ++q) {
-      const float4 w = part[q][threadIdx.x];
-      s.x += w.x;
-      s.y += w.y;
-      s.z += w.z;
-      s.w += w.w;
+#pragma unroll
+  for (int half = 16; half > 0; half >>= 1) {
+    __syncthreads();
+    if (threadIdx.y < half) {
+      const float4 w = part[threadIdx.y + half][threadIdx.x];
+      acc.x += w.x;
+      acc.y += w.y;
+      acc.z += w.z;
+      acc.w += w.w;
+      part[threadIdx.y][threadIdx.x] = acc;
     }
-    reinterpret_cast<float4*>(dst)[c4] = s;
   }
+  if (threadIdx.y == 0 && c4 < n4) reinterpret_cast<float4*>(dst)[c4] = acc;
 }
 
 }  // namespace spf

@@ -344,9 +344,18 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
   for (int st = 0; st < NS; ++st) {
     float* dst = a.ws + ((int64_t)st * a.nparts + blockIdx.x) * H;
     for (int c = threadIdx.x; c < H; c += blockDim.x) {
-      const size_t x = (size_t)(c & (EV - 1)) * pitch + (c / EV);
-      float acc = part[st * plane + x];
-      for (int g = 1; g < nrg; ++g) acc += part[((size_t)g * NS + st) * plane + x];
+      const float* src = part + st * plane + (size_t)(c & (EV - 1)) * pitch + (c / EV);
+      const size_t gstride = (size_t)NS * plane;
+      // row groups in order; the loads of 4 groups are issued before adding
+      float acc = src[0];
+      for (int g0 = 1; g0 < nrg; g0 += 4) {
+        float t[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) t[u] = g0 + u < nrg ? src[(size_t)(g0 + u) * gstride] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (g0 + u < nrg) acc += t[u];
+      }
       __stcg(dst + c, failed ? __int_as_float(0x7FC00000) : acc);
     }
   }

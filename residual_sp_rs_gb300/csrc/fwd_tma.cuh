@@ -161,8 +161,27 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
                 &full[s], pol);
   };
 
+  const bool dropout = a.dropout != 0, nontie = a.dropout && !a.dyadic_scale;
+  const bool last_in = lr + (VPT - 1) * tpr < nvec;  // the last vector slot may fall outside
+  // The mask depends only on the element index: draw (and store) row slot
+  // i's keep bits, before waiting for the row's data.
+  auto draw_row = [&](int i, uint32_t (&keep)[VPT]) {
+    const int64_t r = r0 + i;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      keep[k] = 0xFFu;
+      const int v = lr + k * tpr;
+      if ((FAST || dropout) && i < n && (k < VPT - 1 || last_in)) {
+        const uint64_t g0 = (uint64_t)((a.grow0 + r) * H + (int64_t)v * EV);
+        keep[k] = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
+        if (a.mask) st_mask<EV>(a.mask + r * (int64_t)H + v * EV, keep[k]);
+      }
+    }
+  };
+
   const bool lead = producer && lr == 0;
   int issued = 0;
+  uint32_t keep[VPT];  // keep bits of this thread's next row, drawn ahead
   grid_dep_wait();
   grid_dep_launch_dependents();
   if (lead) {
@@ -173,15 +192,31 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
     fence_mbar_init();
     for (; issued < min(nstage, L.nst); ++issued) issue_stage(issued);
   } else if (!producer) {
-    for (int i = threadIdx.x; i < a.nvec; i += nthr_cons) {
-      float g[EV];
-      Act16<__nv_bfloat16>::unpack(ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV), g);
+    // gamma/beta loads stay in flight while the first row's mask is drawn
+    // (nvec <= VPT * tpr <= VPT * nthr_cons)
+    uint4 gw[VPT], bw[LN ? VPT : 1];
 #pragma unroll
-      for (int e = 0; e < EV; ++e) sgb[i * EV + e] = g[e];
-      if constexpr (LN) {
-        Act16<__nv_bfloat16>::unpack(ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.beta) + i * EV), g);
+    for (int u = 0; u < VPT; ++u) {
+      const int i = threadIdx.x + u * nthr_cons;
+      if (i < nvec) {
+        gw[u] = ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV);
+        if constexpr (LN) bw[u] = ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.beta) + i * EV);
+      }
+    }
+    draw_row(rg, keep);
 #pragma unroll
-        for (int e = 0; e < EV; ++e) sgb[a.H + i * EV + e] = g[e];
+    for (int u = 0; u < VPT; ++u) {
+      const int i = threadIdx.x + u * nthr_cons;
+      if (i < nvec) {
+        float g[EV];
+        Act16<__nv_bfloat16>::unpack(gw[u], g);
+        reinterpret_cast<float4*>(sgb + i * EV)[0] = make_float4(g[0], g[1], g[2], g[3]);
+        reinterpret_cast<float4*>(sgb + i * EV)[1] = make_float4(g[4], g[5], g[6], g[7]);
+        if constexpr (LN) {
+          Act16<__nv_bfloat16>::unpack(bw[u], g);
+          reinterpret_cast<float4*>(sgb + H + i * EV)[0] = make_float4(g[0], g[1], g[2], g[3]);
+          reinterpret_cast<float4*>(sgb + H + i * EV)[1] = make_float4(g[4], g[5], g[6], g[7]);
+        }
       }
     }
   }
@@ -203,8 +238,6 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
 
   float* rred = red + rg * 2 * (tpr >> 5);
   const f2_t shi = f2(a.scale, a.scale), slo = f2(a.scale_lo, a.scale_lo);
-  const bool dropout = a.dropout != 0, nontie = a.dropout && !a.dyadic_scale;
-  const bool last_in = lr + (VPT - 1) * tpr < nvec;  // the last vector slot may fall outside
   // row slot i, its stage j = i / rb, the stage's row ri = i % rb, ring slot
   // s = j % nst and phase parity (j / nst) & 1, kept incrementally
   int ri = rg % L.rb, s = (rg / L.rb) % L.nst, par = ((rg / L.rb) / L.nst) & 1;
@@ -220,20 +253,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
       }
     }
     const int64_t r = r0 + i;
-    const int64_t grow = a.grow0 + r;
 
-    // ---- draw (and store) the row's mask before waiting for its data
-    uint32_t keep[VPT];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      keep[k] = 0xFFu;
-      const int v = lr + k * tpr;
-      if ((FAST || dropout) && i < n && (k < VPT - 1 || last_in)) {
-        const uint64_t g0 = (uint64_t)(grow * H + (int64_t)v * EV);
-        keep[k] = keep_bits4(g0 >> 2, a.keys, a.thr) | (keep_bits4((g0 >> 2) + 1, a.keys, a.thr) << 4);
-        if (a.mask) st_mask<EV>(a.mask + r * (int64_t)H + v * EV, keep[k]);
-      }
-    }
 
     const bool landed = mbar_wait(&full[s], (uint32_t)par);
     const bool all_landed =
@@ -374,6 +394,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
       a.rstd[r] = rstd;
       if constexpr (LN) a.mean[r] = mu;
     }
+    draw_row(i + L.nrg, keep);  // the next row's mask, before its data is waited for
   }
 }
 
