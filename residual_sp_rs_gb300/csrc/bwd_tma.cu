@@ -5,6 +5,9 @@
 #ifndef SPF_BWD_TMA_MIN_COPY
 #define SPF_BWD_TMA_MIN_COPY 16384
 #endif
+#ifndef SPF_BWD_TMA_PREFER_WIDE
+#define SPF_BWD_TMA_PREFER_WIDE 0
+#endif
 #ifndef SPF_BWD_TMA_MAX_BLOCK
 #define SPF_BWD_TMA_MAX_BLOCK 1024
 #endif
@@ -46,7 +49,8 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
   // the narrow block keeps dy and xhat in registers between the passes,
   // which pays more than extra warps unless it leaves a single row group
   int nrg = groups(kBwdTmaNarrow);
-  if (vpt <= 3 && kMaxBlock >= kBwdTmaWide && nrg < 2 && groups(kBwdTmaWide) > nrg)
+  if (vpt <= 3 && kMaxBlock >= kBwdTmaWide && (nrg < 2 || SPF_BWD_TMA_PREFER_WIDE) &&
+      groups(kBwdTmaWide) > nrg)
     nrg = groups(kBwdTmaWide);
   const int ns = ln ? 2 : 1;
   const uint32_t rowb = (uint32_t)H * 2;
@@ -56,8 +60,11 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
     const bool narrow = nrg * tpr + 32 <= kBwdTmaNarrow;
     int rb = (int)((kMinCopy + rowb - 1) / rowb);
     rb = rb < 1 ? 1 : (rb > nrg ? nrg : rb);
-    if (narrow) rb = nrg;  // the narrow kernel walks the ring one stage per row
-    for (; rb >= 1 && (!narrow || rb == nrg); --rb) {
+    // the narrow kernel needs rb to divide nrg (whole stages per round of rows)
+    if (narrow)
+      while (nrg % rb != 0) ++rb;
+    for (; rb >= 1; --rb) {
+      if (narrow && nrg % rb != 0) continue;
       BwdTmaLayout L = {};
       const uint32_t blk = (uint32_t)rb * rowb;  // one tensor's rows in a stage
       L.off_h = blk;

@@ -145,16 +145,17 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
     }
     const f2_t sc = f2(scale, scale);
     // row slot i, its stage j = i / rb, the stage's row ri = i % rb, ring
-    // slot s = j % nst and phase parity (j / nst) & 1.  The 512-thread block
-    // always has rb == nrg (iteration jj is stage jj, ri = rg), which keeps
-    // its register budget; the wide block keeps them incrementally.
+    // slot s = j % nst and phase parity (j / nst) & 1.  In the 512-thread
+    // block rb divides nrg, so iteration jj is stage jj * (nrg / rb) + rg / rb
+    // and ri = rg % rb throughout, which keeps its register budget; the wide
+    // block keeps them incrementally.
     constexpr bool kStageMajor = NTHR <= kBwdTmaNarrowBlock;
     int ri = rg % rb, s = (rg / rb) % nst, par = ((rg / rb) / nst) & 1;
     for (int i = rg, jj = 0; i < nslot; i += nrg, ++jj) {
       if constexpr (kStageMajor) {
-        ri = rg;
-        s = jj % nst;
-        par = (jj / nst) & 1;
+        const int j = jj * (nrg / rb) + rg / rb;
+        s = j % nst;
+        par = (j / nst) & 1;
       } else if (i != rg) {
         ri += nrg;
         while (ri >= rb) {
