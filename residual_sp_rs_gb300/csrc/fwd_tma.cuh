@@ -16,8 +16,13 @@
 //
 // The mask depends only on the element index, so a thread draws (and
 // stores) its row's keep bits before it waits for the row's data: the
-// Philox arithmetic overlaps the loads.  Used when two stages fit in shared
-// memory; longer rows (T*H large) take the register-resident kernel.
+// Philox arithmetic overlaps the loads.
+//
+// CH (chunked): when a stage of one whole row does not fit twice in shared
+// memory (T*H large), a stage holds one column chunk of one row instead --
+// the tpr vectors of one vector slot k of every thread (tpr*16 bytes of each
+// input) -- so a row is VPT stages, each released as soon as its slot's h is
+// in registers.
 //
 // If a wait times out, the row group stops and writes NaN into the rstd of
 // the rows it did not finish, so the failure is visible in the outputs.
@@ -121,9 +126,10 @@ struct HRow<VPT, true> {
   __device__ __forceinline__ f2_t get(int k, int q) const { return bf2_to_f2(w[k][q]); }
 };
 
-template <int T, bool LN, int VPT, bool FAST, int NTHR>
+template <int T, bool LN, int VPT, bool FAST, int NTHR, bool CH>
 __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, const FwdTmaLayout L) {
   constexpr int EV = 8;
+  constexpr int NCH = CH ? VPT : 1;  // stages per row stage (CH: rb == 1)
   constexpr bool kPackH = NTHR > 544;
   __shared__ float red[2 * 32 * 2];
   extern __shared__ __align__(16) unsigned char dsm[];
@@ -141,23 +147,31 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
   const int64_t r0 = (int64_t)blockIdx.x * L.rows_per_cta;
   const int64_t r1 = min(a.rows, r0 + L.rows_per_cta);
   const int n = r1 > r0 ? (int)(r1 - r0) : 0;
-  const int nstage = (n + L.rb - 1) / L.rb;
-  const int nslot = nstage * L.rb;  // row slots, the last stage padded to rb rows
+  const int nrow_st = (n + L.rb - 1) / L.rb;  // stages of rb rows (CH: rows)
+  const int nstage = nrow_st * NCH;
+  const int nslot = nrow_st * L.rb;  // row slots, the last stage padded to rb rows
   const size_t rowb = (size_t)H * 2;
   const uint64_t pol = policy_evict_first();
 
   auto issue_stage = [&](int j) {
     const int s = j % L.nst;
     unsigned char* st = stages + (size_t)s * L.stage_bytes;
-    const int64_t r = r0 + (int64_t)j * L.rb;  // local row of the stage's first row
-    const int rows = min(L.rb, n - j * L.rb);
-    const uint32_t bb = (uint32_t)(rows * rowb);
+    const int jr = j / NCH, k = j - jr * NCH;   // row stage and (CH) column chunk
+    const int64_t r = r0 + (int64_t)jr * L.rb;  // local row of the stage's first row
+    size_t off = 0;
+    uint32_t bb;
+    if constexpr (CH) {
+      off = (size_t)k * L.blk;
+      bb = (uint32_t)min((size_t)L.blk, rowb - off);
+    } else {
+      bb = (uint32_t)(min(L.rb, n - jr * L.rb) * rowb);
+    }
     mbar_arrive_expect_tx(&full[s], bb * (uint32_t)(T + 1));
 #pragma unroll
     for (int t = 0; t < T; ++t)
-      tma_load_1d(st + (size_t)t * L.blk, reinterpret_cast<const char*>(a.P[t]) + (a.grow0 + r) * rowb,
-                  bb, &full[s], pol);
-    tma_load_1d(st + (size_t)T * L.blk, reinterpret_cast<const char*>(a.residual) + r * rowb, bb,
+      tma_load_1d(st + (size_t)t * L.blk,
+                  reinterpret_cast<const char*>(a.P[t]) + (a.grow0 + r) * rowb + off, bb, &full[s], pol);
+    tma_load_1d(st + (size_t)T * L.blk, reinterpret_cast<const char*>(a.residual) + r * rowb + off, bb,
                 &full[s], pol);
   };
 
@@ -238,36 +252,43 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
 
   float* rred = red + rg * 2 * (tpr >> 5);
   const f2_t shi = f2(a.scale, a.scale), slo = f2(a.scale_lo, a.scale_lo);
-  // row slot i, its stage j = i / rb, the stage's row ri = i % rb, ring slot
-  // s = j % nst and phase parity (j / nst) & 1, kept incrementally
-  int ri = rg % L.rb, s = (rg / L.rb) % L.nst, par = ((rg / L.rb) / L.nst) & 1;
+  // row slot i, its row stage jr = i / rb, the stage's row ri = i % rb, the
+  // ring slot s = (jr * NCH) % nst of its first stage and that stage's phase
+  // parity ((jr * NCH) / nst) & 1, kept incrementally
+  int ri = rg % L.rb, s = ((rg / L.rb) * NCH) % L.nst, par = (((rg / L.rb) * NCH) / L.nst) & 1;
+  // wait for ring slot (s, par) -- the whole row group agrees -- or give up
+  auto wait_stage = [&](int ws, int wpar, int i) -> bool {
+    const bool landed = mbar_wait(&full[ws], (uint32_t)wpar);
+    const bool all_landed =
+        tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
+    if (!all_landed) {  // mark this row group's unfinished rows
+      for (int k = i; k < n; k += L.nrg)
+        if (lr == 0) a.rstd[r0 + k] = __int_as_float(0x7FC00000);
+    }
+    return all_landed;
+  };
   for (int i = rg; i < nslot; i += L.nrg) {
     if (i != rg) {
       ri += L.nrg;
       while (ri >= L.rb) {
         ri -= L.rb;
-        if (++s == L.nst) {
-          s = 0;
-          par ^= 1;
-        }
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+          if (++s == L.nst) {
+            s = 0;
+            par ^= 1;
+          }
       }
     }
     const int64_t r = r0 + i;
 
-
-    const bool landed = mbar_wait(&full[s], (uint32_t)par);
-    const bool all_landed =
-        tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
-    if (!all_landed) {  // give up: mark this row group's remaining rows
-      for (int k = i; k < n; k += L.nrg)
-        if (lr == 0) a.rstd[r0 + k] = __int_as_float(0x7FC00000);
-      return;
-    }
-    if (i >= n) {  // padding of the last stage
-      mbar_arrive(&empty[s]);
+    if (!CH && !wait_stage(s, par, i)) return;
+    if (i >= n) {  // padding of the last stage (never with CH: rb == 1)
+      if constexpr (!CH) mbar_arrive(&empty[s]);
       continue;
     }
     const unsigned char* st = stages + (size_t)s * L.stage_bytes + (size_t)ri * rowb;
+    int cs = s, cpar = par;  // CH: the ring slot of column chunk k
     __nv_bfloat16* h_row = reinterpret_cast<__nv_bfloat16*>(a.h) + r * (int64_t)H;
     __nv_bfloat16* y_row = reinterpret_cast<__nv_bfloat16*>(a.y) + r * (int64_t)H;
 
@@ -279,11 +300,23 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lr + k * tpr;
+      // this thread's vector of slot k: vector vi of each tensor block at sb
+      const unsigned char* sb = st;
+      int vi = v;
+      if constexpr (CH) {
+        if (k > 0 && ++cs == L.nst) {
+          cs = 0;
+          cpar ^= 1;
+        }
+        if (!wait_stage(cs, cpar, i)) return;
+        sb = stages + (size_t)cs * L.stage_bytes;
+        vi = lr;
+      }
       if (k < VPT - 1 || last_in) {
         uint4 pw[T];
 #pragma unroll
-        for (int t = 0; t < T; ++t) pw[t] = reinterpret_cast<const uint4*>(st + (size_t)t * L.blk)[v];
-        const uint4 rw = reinterpret_cast<const uint4*>(st + (size_t)T * L.blk)[v];
+        for (int t = 0; t < T; ++t) pw[t] = reinterpret_cast<const uint4*>(sb + (size_t)t * L.blk)[vi];
+        const uint4 rw = reinterpret_cast<const uint4*>(sb + (size_t)T * L.blk)[vi];
         const uint32_t kb = keep[k];
         uint32_t hw[4];
         if constexpr (FAST) {
@@ -327,8 +360,9 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
         }
         st_stream(h_row + v * EV, make_uint4(hw[0], hw[1], hw[2], hw[3]));
       }
+      if constexpr (CH) mbar_arrive(&empty[cs]);  // this chunk is no longer read
     }
-    mbar_arrive(&empty[s]);  // the stage is no longer read
+    if constexpr (!CH) mbar_arrive(&empty[s]);  // the stage is no longer read
 
     // ---- row statistics -----------------------------------------------------
     float sv[1];

@@ -1,9 +1,10 @@
-// TMA-fed forward instances: bf16, norm ln.
+// TMA-fed forward instances: bf16, norm ln, whole-row stages.
 #include "fwd_tma_inst.cuh"
 
 namespace spf {
 cudaError_t launch_fwd_tma_ln(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid,
                                 cudaStream_t st) {
-  return launch_fwd_tma_impl<true>(a, T, p, grid, st);
+  if (p.chunked) return launch_fwd_tma_ln_ch(a, T, p, grid, st);
+  return launch_fwd_tma_impl<true, false>(a, T, p, grid, st);
 }
 }  // namespace spf

@@ -30,8 +30,9 @@ int ring_stages(size_t stage, size_t gb, size_t budget) {
 // Picks the narrowest row group (<= 3 vectors per thread), as many row groups
 // as the block size allows but no more than the rows a CTA owns, and stages
 // of rb rows (copies of at least kMinCopy bytes where the ring allows), as
-// many as fit in shared memory next to gamma/beta (at least two); false when
-// two one-row stages do not fit (long rows).  T <= 4 takes the 1024-thread
+// many as fit in shared memory next to gamma/beta (at least two).  When two
+// one-row stages do not fit (T*H large), stages of one column chunk of a row;
+// false when not even those fit.  T <= 4 takes the 1024-thread
 // block (more rows in flight per SM); larger T the 544-thread one, which
 // leaves each thread more registers.
 bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms, FwdTmaPlan* p) {
@@ -56,14 +57,25 @@ bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms
       nst = ring_stages((size_t)rb * (T + 1) * rowb, gb, budget);
       if (nst >= 2) break;
     }
-    if (rb < 1) return false;  // wider row groups do not shorten the rows
-    const size_t stage = (size_t)rb * (T + 1) * rowb;
+    bool chunked = false;
+    size_t blk = (size_t)rb * rowb, stage = blk * (T + 1);
+    if (rb < 1) {
+      // a whole row does not fit twice: stages of one column chunk (one
+      // vector slot of the row group, tpr*16 bytes of each input)
+      if (vpt < 2) return false;
+      rb = 1;
+      blk = (size_t)tpr * 16;
+      stage = blk * (T + 1);
+      nst = ring_stages(stage, gb, budget);
+      if (nst < 2) return false;
+      chunked = true;
+    }
     FwdTmaLayout L = {};
     L.nst = nst;
     L.nrg = nrg;
     L.rb = rb;
     L.stage_bytes = (uint32_t)stage;
-    L.blk = (uint32_t)(rb * rowb);
+    L.blk = (uint32_t)blk;
     L.smem_stages = (uint32_t)(16 * (((size_t)2 * nst * 8 + 15) / 16) + gb);
     L.rows_per_cta = rows_per_cta;
     p->layout = L;
@@ -71,6 +83,7 @@ bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms
     p->shape.vpt = vpt;
     p->shape.block = nrg * tpr + 32;
     p->nthr = wide ? kFwdTmaWide : kFwdTmaDeep;
+    p->chunked = chunked;
     p->smem = L.smem_stages + (size_t)nst * stage;
     return true;
   }

@@ -84,12 +84,15 @@ constexpr int kFwdTmaWideMaxT = 4;
 struct FwdTmaPlan {
   RowShape shape;
   size_t smem;
-  int nthr;  // kFwdTmaDeep or kFwdTmaWide
+  int nthr;     // kFwdTmaDeep or kFwdTmaWide
+  bool chunked;  // stages of one column chunk of one row
   FwdTmaLayout layout;
 };
 bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms, FwdTmaPlan* p);
 cudaError_t launch_fwd_tma_rms(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid, cudaStream_t st);
 cudaError_t launch_fwd_tma_ln(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_tma_rms_ch(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid, cudaStream_t st);
+cudaError_t launch_fwd_tma_ln_ch(const FwdArgs& a, int T, const FwdTmaPlan& p, dim3 grid, cudaStream_t st);
 
 cudaError_t launch_layout(bool to_hp, const void* in, void* out, int64_t N, int64_t H, int32_t T,
                           int elem_bytes, cudaStream_t stream);

@@ -150,6 +150,10 @@ def test_fwd_large_hidden_every_shard_sampled(p):
     (2, 4, 5, 8192, "f32", "ln", 0.1),
     (4, 8, 3, 12, "f32", "rms", 0.7),
     (7, 14, 1, 1032, "f32", "ln", 0.0),
+    # rows too long for a whole-row ring stage: column-chunk stages, one ragged
+    (8, 16, 1, 8200, "bf16", "rms", 0.1),
+    (8, 8, 2, 8192, "bf16", "ln", 0.1),
+    (4, 8, 2, 12288, "bf16", "rms", 0.5),
 ])
 def test_fwd_edge_shapes(case):
     T, S, B, H, dt, nm, p = case
