@@ -71,25 +71,16 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-#ifndef SPF_WAIT_MODE
-#define SPF_WAIT_MODE 1
-#endif
-
 // Wait for the phase with the given parity to complete; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-#if SPF_WAIT_MODE == 1
+  // the clock is read once per 64 polls: %globaltimer read in a tight loop
+  // on many SMs slows every reader of it
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
+    if ((i & 63u) == 63u && global_ns() - t0 > kWaitNs) return false;
   }
-#else
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(64);
-  }
-#endif
   return false;
 }
 
