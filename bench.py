@@ -357,7 +357,7 @@ def run_ours(args):
     # ---- end to end: pinned host inputs in, results out, every step -------------
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, desc, dev, sets[0], rows, world)
+        e2e = run_e2e(args, w, desc, dev, sets, rows, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -389,50 +389,73 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, desc, dev, s, rows, world):
+def run_e2e(args, w, desc, dev, sets, rows, world):
     """Through the public API with HOST buffers: every step copies its inputs
-    from pinned host memory, runs the step and reads the results back."""
+    from pinned host memory, runs the step and copies its results back.  The
+    steps run as a three-stage pipeline on two device buffer sets (inputs in
+    on one stream, the step on a second, results out on a third), so one
+    step's copies overlap the neighbouring steps' compute and copies, as in a
+    training loop that prefetches its next batch."""
     import torch
 
     from residual_sp_rs_gb300 import ops
 
     T, H = w.T, w.H
-    host_in = {k: s[k].cpu().pin_memory() for k in ("residual", "dy", "dh", "gamma")}
-    host_parts = [p.view(rows, H).cpu().pin_memory() for p in s["partials"]]
+    dsets = sets[:2]
+    s0 = dsets[0]
+    host_in = {k: s0[k].cpu().pin_memory() for k in ("residual", "dy", "dh", "gamma")}
+    host_parts = [p.view(rows, H).cpu().pin_memory() for p in s0["partials"]]
     outs = ("y", "d_res", "d_sum", "dgamma")
-    host_out = {k: torch.empty(s[k].shape, dtype=s[k].dtype, pin_memory=True) for k in outs}
+    host_out = {k: torch.empty(s0[k].shape, dtype=s0[k].dtype, pin_memory=True) for k in outs}
     bi = sum(v.numel() * v.element_size() for v in host_in.values()) + \
         sum(v.numel() * v.element_size() for v in host_parts)
     bo = sum(v.numel() * v.element_size() for v in host_out.values())
+    st_in, st_cmp, st_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in dsets]
+    ev_cmp = [torch.cuda.Event() for _ in dsets]
+    ev_out = [torch.cuda.Event() for _ in dsets]
 
-    def one_step():
-        for k, v in host_in.items():
-            s[k].copy_(v, non_blocking=True)
-        for p, hp in zip(s["partials"], host_parts):
-            p.view(rows, H).copy_(hp, non_blocking=True)
-        ops.sp_rs_dropout_residual_norm_fwd(desc, s["partials"], s["residual"], s["gamma"], s["beta"],
-                                            s["h"], s["y"], s["mask"], s["rstd"], s["mean"])
-        ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype)
-        ops.hp2sp(s["y_hp"], s["y_sp"], rows, H, T, w.dtype)
-        ops.sp_rs_dropout_residual_norm_bwd(desc, s["dy"], s["dh"], s["h"], s["gamma"], s["mask"],
-                                            s["rstd"], s["mean"], s["d_res"], s["d_sum"], s["dgamma"],
-                                            s["dbeta"], s["ws"])
-        for k in outs:
-            host_out[k].copy_(s[k], non_blocking=True)
+    def one_step(i):
+        k = i % len(dsets)
+        s = dsets[k]
+        st_in.wait_event(ev_cmp[k])  # the set's inputs are free once its last step ran
+        with torch.cuda.stream(st_in):
+            for name, v in host_in.items():
+                s[name].copy_(v, non_blocking=True)
+            for p, hp in zip(s["partials"], host_parts):
+                p.view(rows, H).copy_(hp, non_blocking=True)
+            ev_in[k].record(st_in)
+        st_cmp.wait_event(ev_in[k])
+        st_cmp.wait_event(ev_out[k])  # the set's outputs are free once copied out
+        with torch.cuda.stream(st_cmp):
+            ops.sp_rs_dropout_residual_norm_fwd(desc, s["partials"], s["residual"], s["gamma"], s["beta"],
+                                                s["h"], s["y"], s["mask"], s["rstd"], s["mean"])
+            ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype)
+            ops.hp2sp(s["y_hp"], s["y_sp"], rows, H, T, w.dtype)
+            ops.sp_rs_dropout_residual_norm_bwd(desc, s["dy"], s["dh"], s["h"], s["gamma"], s["mask"],
+                                                s["rstd"], s["mean"], s["d_res"], s["d_sum"],
+                                                s["dgamma"], s["dbeta"], s["ws"])
+            ev_cmp[k].record(st_cmp)
+        st_out.wait_event(ev_cmp[k])
+        with torch.cuda.stream(st_out):
+            for name in outs:
+                host_out[name].copy_(s[name], non_blocking=True)
+            ev_out[k].record(st_out)
 
-    for _ in range(5):
-        one_step()
+    for i in range(6):
+        one_step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.e2e_steps):
-        one_step()
-    b.record()
+    a.record(st_in)
+    for i in range(args.e2e_steps):
+        one_step(i)
+    b.record(st_out)  # after the last step's results are on the host
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
     return {"value": round(rows * args.e2e_steps * world / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps,
-            "ms_per_step": round(ms / args.e2e_steps, 5)}
+            "ms_per_step": round(ms / args.e2e_steps, 5),
+            "pipeline": "copy-in / step / copy-out on three streams over two device buffer sets"}
 
 
 # ---------------------------------------------------------------------------
