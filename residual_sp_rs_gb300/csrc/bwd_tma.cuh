@@ -259,8 +259,19 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
           const float4* gp = reinterpret_cast<const float4*>(sgam + v * EV);
           uint4 wdh = make_uint4(0u, 0u, 0u, 0u);
           if constexpr (DH) wdh = sdh[v];
+          // the stored mask is applied to the packed bf16 output as byte
+          // masks in the 16-warp block; the wide block (fewer registers) and
+          // the regenerated mask use keep bits
+          constexpr bool kByteMask = MASK && NTHR <= kBwdTmaNarrowBlock;
           uint32_t mk = 0xFFu;
-          if constexpr (MASK) mk = ld_mask_shared8(smk + v * EV);
+          uint2 mbytes = make_uint2(0u, 0u);  // each mask byte as 0x00 / 0xFF
+          if constexpr (kByteMask) {
+            mbytes = *reinterpret_cast<const uint2*>(smk + v * EV);
+            mbytes.x = (mbytes.x & 0x01010101u) * 0xFFu;
+            mbytes.y = (mbytes.y & 0x01010101u) * 0xFFu;
+          } else if constexpr (MASK) {
+            mk = ld_mask_shared8(smk + v * EV);
+          }
           if constexpr (REGEN) mk = keep[k];
           uint4 wdy2 = make_uint4(0u, 0u, 0u, 0u), wh2 = make_uint4(0u, 0u, 0u, 0u);
           if constexpr (!KEEP) {
@@ -289,13 +300,19 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
             else
               dres = f2_mul(r2, t);
             f2_t dsum = f2_mul(dres, sc);
-            if constexpr (MASK || REGEN) {
+            if constexpr ((MASK && !kByteMask) || REGEN) {
               float sl, sh2;
               f2_split(dsum, sl, sh2);
               dsum = f2(((mk >> (2 * q)) & 1u) ? sl : 0.f, ((mk >> (2 * q + 1)) & 1u) ? sh2 : 0.f);
             }
             wres[q] = f2_to_bf2(dres);
             wsum[q] = f2_to_bf2(dsum);
+            if constexpr (kByteMask) {
+              // a dropped element's bf16 becomes +0, as if its product were 0:
+              // the 16-bit halves take the 0x00/0xFF bytes of elements 2q, 2q+1
+              const uint32_t mb = (q < 2) ? mbytes.x : mbytes.y;
+              wsum[q] &= __byte_perm(mb, 0u, (q & 1) ? 0x3322u : 0x1100u);
+            }
             dg[k][q] = f2_fma(dy, xh, dg[k][q]);
             if constexpr (LN) db[k][q] = f2_add(db[k][q], dy);
           }
