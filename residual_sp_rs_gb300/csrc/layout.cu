@@ -3,7 +3,8 @@
 // and the hidden-split layout [N, H/T] per rank, as one permutation copy on
 // a GPU that holds all T rank buffers.
 //
-// Each thread moves VPT 16-byte vectors, issuing all loads before any store.
+// Each thread moves kLayoutVPT 16-byte vectors, issuing all loads before any
+// store.
 // sp2hp walks the INPUT in order (coalesced reads; a warp's writes stay
 // inside one destination chunk of H/T elements except at chunk edges);
 // hp2sp walks the OUTPUT in order.  Index math is 32-bit when the vector
@@ -16,7 +17,7 @@ namespace spf {
 namespace {
 
 constexpr int kLayoutThreads = 256;
-constexpr int kLayoutVPT = 4;
+constexpr int kLayoutVPT = 2;  // 2-4 measure alike; 8 (fewer CTAs) is slower
 
 // nv: vectors per [N,H] row; ncv: vectors per H/T chunk.
 template <bool TO_HP, typename Idx>
