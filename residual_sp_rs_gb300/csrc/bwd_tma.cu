@@ -2,15 +2,6 @@
 // 16) and its launch.
 #include "launch.h"
 
-#ifndef SPF_BWD_TMA_MIN_COPY
-#define SPF_BWD_TMA_MIN_COPY 16384
-#endif
-#ifndef SPF_BWD_TMA_PREFER_WIDE
-#define SPF_BWD_TMA_PREFER_WIDE 0
-#endif
-#ifndef SPF_BWD_TMA_MAX_BLOCK
-#define SPF_BWD_TMA_MAX_BLOCK 1024
-#endif
 
 namespace spf {
 
@@ -20,8 +11,7 @@ constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, roun
 constexpr int kMaxStages = 32;
 // smallest bulk copy worth issuing: a stage takes enough rows that its dy
 // copy moves at least this many bytes (up to one row per group)
-constexpr size_t kMinCopy = SPF_BWD_TMA_MIN_COPY;
-constexpr int kMaxBlock = SPF_BWD_TMA_MAX_BLOCK;
+constexpr size_t kMinCopy = 16384;
 
 }  // namespace
 
@@ -49,8 +39,7 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
   // the narrow block keeps dy and xhat in registers between the passes,
   // which pays more than extra warps unless it leaves a single row group
   int nrg = groups(kBwdTmaNarrow);
-  if (vpt <= 3 && kMaxBlock >= kBwdTmaWide && (nrg < 2 || SPF_BWD_TMA_PREFER_WIDE) &&
-      groups(kBwdTmaWide) > nrg)
+  if (vpt <= 3 && nrg < 2 && groups(kBwdTmaWide) > nrg)
     nrg = groups(kBwdTmaWide);
   const int ns = ln ? 2 : 1;
   const uint32_t rowb = (uint32_t)H * 2;

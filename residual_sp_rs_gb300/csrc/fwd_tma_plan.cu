@@ -3,20 +3,13 @@
 
 namespace spf {
 
-#ifndef SPF_FWD_TMA_MIN_COPY
-#define SPF_FWD_TMA_MIN_COPY 8192
-#endif
-#ifndef SPF_FWD_TMA_MAX_BLOCK
-#define SPF_FWD_TMA_MAX_BLOCK 1024
-#endif
 
 namespace {
 constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, rounded up
 constexpr int kMaxStages = 48;
 // smallest bulk copy worth issuing: a stage takes enough rows that each of
 // its T+1 copies moves at least this many bytes (up to one row per group)
-constexpr size_t kMinCopy = SPF_FWD_TMA_MIN_COPY;
-constexpr int kMaxBlock = SPF_FWD_TMA_MAX_BLOCK;
+constexpr size_t kMinCopy = 8192;
 
 int ring_stages(size_t stage, size_t gb, size_t budget) {
   for (int cand = kMaxStages; cand >= 2; --cand) {
@@ -42,7 +35,7 @@ bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms
   const size_t budget = (size_t)max_smem - kStaticSmem;
   const int64_t ctas = rows < sms ? (rows > 0 ? rows : 1) : sms;
   const int64_t rows_per_cta = rows > 0 ? (rows + ctas - 1) / ctas : 1;
-  const bool wide = T <= kFwdTmaWideMaxT && kMaxBlock >= kFwdTmaWide;
+  const bool wide = T <= kFwdTmaWideMaxT;
   const int cons_warps = (wide ? kFwdTmaWide : kFwdTmaDeep) / 32 - 1;
   for (int tpr = 32; tpr / 32 <= cons_warps; tpr *= 2) {
     const int vpt = (nvec + tpr - 1) / tpr;

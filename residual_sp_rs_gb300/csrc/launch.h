@@ -56,11 +56,8 @@ cudaError_t launch_colsum(const float* ws, int nparts, int H, bool ln, float* dg
 // TMA-fed backward (bf16, H % 16 == 0): shared-memory ring layout and shape.
 // Block sizes the TMA backward is compiled for: 15 consumer warps + producer
 // (128 registers), or 23 + producer (80 registers, up to 3 vectors a thread).
-#ifndef SPF_BWD_TMA_WIDE
-#define SPF_BWD_TMA_WIDE 768
-#endif
 constexpr int kBwdTmaNarrow = 512;
-constexpr int kBwdTmaWide = SPF_BWD_TMA_WIDE;
+constexpr int kBwdTmaWide = 768;
 
 struct BwdTmaPlan {
   RowShape shape;
