@@ -2,7 +2,6 @@
 // 16) and its launch.
 #include "launch.h"
 
-
 namespace spf {
 
 namespace {

@@ -3,7 +3,6 @@
 
 namespace spf {
 
-
 namespace {
 constexpr size_t kStaticSmem = 1024;  // the kernel's static shared arrays, rounded up
 constexpr int kMaxStages = 48;
