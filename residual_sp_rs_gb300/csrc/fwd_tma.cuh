@@ -11,8 +11,8 @@
 // one row overlaps the loads of the next ones.  Small stages (down to one
 // row) let the first rows start as soon as they land.  gamma/beta are kept
 // in shared memory as fp32.  NTHR is the block size the registers are
-// budgeted for: 544 (16 consumer warps + producer, up to 120 registers) or
-// 1024 (64 registers) for the many short rows of small T.
+// budgeted for: 544 (16 consumer warps + producer, up to 96 registers) or
+// 896 (27 + producer, 72 registers) for the many short rows of small T.
 //
 // The mask depends only on the element index, so a thread draws (and
 // stores) its row's keep bits before it waits for the row's data: the
@@ -130,7 +130,7 @@ template <int T, bool LN, int VPT, bool FAST, int NTHR, bool CH>
 __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, const FwdTmaLayout L) {
   constexpr int EV = 8;
   constexpr int NCH = CH ? VPT : 1;  // stages per row stage (CH: rb == 1)
-  constexpr bool kPackH = NTHR > 544;
+  constexpr bool kPackH = NTHR > 896;  // fewer than 72 registers: keep h as bf16 pairs
   __shared__ float red[2 * 32 * 2];
   extern __shared__ __align__(16) unsigned char dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
     __nv_bfloat16* y_row = reinterpret_cast<__nv_bfloat16*>(a.y) + r * (int64_t)H;
 
     // ---- reduce, dropout, residual add; store h ----------------------------
-    // h stays in registers for the norm: as fp32 pairs, or (1024-thread
-    // block, 64 registers) as the stored bf16 pairs, unpacked again per use
+    // h stays in registers for the norm: as fp32 pairs (or, under a tighter
+    // register budget, as the stored bf16 pairs, unpacked again per use)
     HRow<VPT, kPackH> hf;
     f2_t s2 = f2(0.f, 0.f);
 #pragma unroll

@@ -1,6 +1,6 @@
 // fwd_tma_inst.cuh -- instances of the TMA-fed forward for one norm over
 // T = 1..8, VPT = 1..3, the fast / generic rounding mode, the two block
-// sizes (the 1024-thread one only for T <= 4) and whole-row or column-chunk
+// sizes (the 896-thread one only for T <= 4) and whole-row or column-chunk
 // stages (one translation unit each).
 #pragma once
 

@@ -24,7 +24,7 @@ int ring_stages(size_t stage, size_t gb, size_t budget) {
 // of rb rows (copies of at least kMinCopy bytes where the ring allows), as
 // many as fit in shared memory next to gamma/beta (at least two).  When two
 // one-row stages do not fit (T*H large), stages of one column chunk of a row;
-// false when not even those fit.  T <= 4 takes the 1024-thread
+// false when not even those fit.  T <= 4 takes the 896-thread
 // block (more rows in flight per SM); larger T the 544-thread one, which
 // leaves each thread more registers.
 bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms, FwdTmaPlan* p) {

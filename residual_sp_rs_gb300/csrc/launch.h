@@ -73,9 +73,9 @@ cudaError_t launch_bwd_tma_ln(const BwdArgs& a, const BwdTmaPlan& p, dim3 grid, 
 
 // TMA-fed forward (bf16, rows short enough for a two-stage ring).
 // Block sizes the TMA forward is compiled for: 16 consumer warps + producer
-// (registers for T up to 8), or 31 + producer (64 registers, T <= 4).
+// (registers for T up to 8), or 27 + producer (72 registers, T <= 4).
 constexpr int kFwdTmaDeep = 544;
-constexpr int kFwdTmaWide = 1024;
+constexpr int kFwdTmaWide = 896;
 constexpr int kFwdTmaWideMaxT = 4;
 
 struct FwdTmaPlan {
