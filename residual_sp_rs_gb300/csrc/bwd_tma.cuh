@@ -207,9 +207,10 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
       }
       const f2_t r2 = f2(rstd, rstd), mu2 = f2(mu, mu);
 
-      // pass 1: dy and xhat = (h-mu)*rstd to registers; row sums of g*xhat
-      // (and g), g = gamma*dy
-      f2_t dyk[KEEP ? VPT : 1][4], xhk[KEEP ? VPT : 1][4];
+      // pass 1: xhat = (h-mu)*rstd and g = gamma*dy; row sums of g*xhat (and
+      // g); the dgamma/dbeta contributions dy*xhat (and dy).  With KEEP, g and
+      // xhat stay in registers for pass 2.
+      f2_t gk[KEEP ? VPT : 1][4], xhk[KEEP ? VPT : 1][4];
       f2_t sgx = f2(0.f, 0.f), sg = f2(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -222,12 +223,15 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
             const float4 g4 = gp[q >> 1];
             const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
             const f2_t dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]);
-            const f2_t xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]), mu2), r2);
-            if constexpr (KEEP) {
-              dyk[k][q] = dy;
-              xhk[k][q] = xh;
-            }
+            const f2_t hq = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]);
+            const f2_t xh = (KEEP && !LN) ? f2_mul(hq, r2) : f2_mul(f2_sub(hq, mu2), r2);  // RMS: mean 0
             const f2_t g = f2_mul(gm, dy);
+            if constexpr (KEEP) {
+              gk[k][q] = g;
+              xhk[k][q] = xh;
+              dg[k][q] = f2_fma(dy, xh, dg[k][q]);
+              if constexpr (LN) db[k][q] = f2_add(db[k][q], dy);
+            }
             sgx = f2_fma(g, xh, sgx);
             if constexpr (LN) sg = f2_add(sg, g);
           }
@@ -249,7 +253,8 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
       const float cgs = LN ? sums[NS - 1] * invH : 0.f;
       const f2_t cg = f2(cgs, cgs);
 
-      // pass 2: dH, d_residual, d_sum; dgamma/dbeta contributions
+      // pass 2: dH, d_residual, d_sum (without KEEP also the dgamma/dbeta
+      // contributions, from dy and h read again)
       __nv_bfloat16* dres_row = reinterpret_cast<__nv_bfloat16*>(a.d_res) + r * (int64_t)H;
       __nv_bfloat16* dsum_row = reinterpret_cast<__nv_bfloat16*>(a.d_sum) + r * (int64_t)H;
 #pragma unroll
@@ -281,19 +286,19 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
           uint32_t wres[4], wsum[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float4 g4 = gp[q >> 1];
-            const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
-            f2_t dy, xh;
+            f2_t g, xh, dy;
             if constexpr (KEEP) {
-              dy = dyk[k][q];
+              g = gk[k][q];
               xh = xhk[k][q];
             } else {
+              const float4 g4 = gp[q >> 1];
+              const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
               dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy2)[q]);
               xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh2)[q]), mu2), r2);
+              g = f2_mul(gm, dy);
             }
-            const f2_t g = f2_mul(gm, dy);
             // rstd * (g - mean(g) - xhat * mean(g xhat)) + dh_out
-            const f2_t t = f2_fma(xh, ncgx, f2_sub(g, cg));
+            const f2_t t = (KEEP && !LN) ? f2_fma(xh, ncgx, g) : f2_fma(xh, ncgx, f2_sub(g, cg));
             f2_t dres;
             if constexpr (DH)
               dres = f2_fma(r2, t, bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdh)[q]));
@@ -313,8 +318,10 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
               const uint32_t mb = (q < 2) ? mbytes.x : mbytes.y;
               wsum[q] &= __byte_perm(mb, 0u, (q & 1) ? 0x3322u : 0x1100u);
             }
-            dg[k][q] = f2_fma(dy, xh, dg[k][q]);
-            if constexpr (LN) db[k][q] = f2_add(db[k][q], dy);
+            if constexpr (!KEEP) {
+              dg[k][q] = f2_fma(dy, xh, dg[k][q]);
+              if constexpr (LN) db[k][q] = f2_add(db[k][q], dy);
+            }
           }
           st_stream(dres_row + v * EV, make_uint4(wres[0], wres[1], wres[2], wres[3]));
           st_stream(dsum_row + v * EV, make_uint4(wsum[0], wsum[1], wsum[2], wsum[3]));
