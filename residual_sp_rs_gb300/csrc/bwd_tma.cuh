@@ -82,6 +82,16 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
   };
   const bool lead = producer && lr == 0;
   int issued = 0;
+  if (lead && n > 0 && n <= nst * rb) {
+    // the CTA's rows all fit the first ring: they head for L2 while the
+    // previous kernel drains (with more rows per CTA the start-up is a small
+    // share of the kernel and the early requests only compete with it)
+    const uint32_t pb = (uint32_t)(n * rowb);
+    l2_prefetch(reinterpret_cast<const char*>(a.dy) + r0 * rowb, pb);
+    l2_prefetch(reinterpret_cast<const char*>(a.h) + r0 * rowb, pb);
+    if constexpr (DH) l2_prefetch(reinterpret_cast<const char*>(a.dh) + r0 * rowb, pb);
+    if constexpr (MASK) l2_prefetch(a.mask + r0 * (int64_t)H, (uint32_t)(n * H));
+  }
   grid_dep_wait();
   grid_dep_launch_dependents();
   if (lead) {

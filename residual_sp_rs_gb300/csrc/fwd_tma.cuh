@@ -196,6 +196,15 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
   const bool lead = producer && lr == 0;
   int issued = 0;
   uint32_t keep[VPT];  // keep bits of this thread's next row, drawn ahead
+  if (!CH && lead && n > 0 && n <= L.nst * L.rb) {
+    // the CTA's rows all fit the first ring: they head for L2 while the
+    // previous kernel drains (with more rows per CTA the start-up is a small
+    // share of the kernel and the early requests only compete with it)
+    const uint32_t pb = (uint32_t)(n * rowb);
+#pragma unroll
+    for (int t = 0; t < T; ++t) l2_prefetch(reinterpret_cast<const char*>(a.P[t]) + (a.grow0 + r0) * rowb, pb);
+    l2_prefetch(reinterpret_cast<const char*>(a.residual) + r0 * rowb, pb);
+  }
   grid_dep_wait();
   grid_dep_launch_dependents();
   if (lead) {

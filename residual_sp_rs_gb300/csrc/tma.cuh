@@ -96,6 +96,14 @@ __device__ __forceinline__ void tma_load_1d(void* dst_smem, const void* src, uin
       : "memory");
 }
 
+// Start bringing `bytes` (a multiple of 16) of global memory at a 16-byte
+// aligned address into L2, without waiting.  A hint only: a later load of
+// the same bytes reads what is current, so it may go out before the kernel
+// that writes them has finished (L2 is the device's point of coherence).
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
