@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -307,20 +308,38 @@ def run_ours(args):
         with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="relaxed"):
             for i in range(per_graph):
                 fn(sets[i % n_sets])
-        g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
+        for _ in range(3):
             g.replay()
-        b.record()
         torch.cuda.synchronize()
-        return a.elapsed_time(b) / (reps * per_graph)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        evs[0].record()
+        for i in range(reps):
+            g.replay()
+            evs[i + 1].record()
+        torch.cuda.synchronize()
+        # median over replays of the mean launch duration within a replay
+        return float(np.median([evs[i].elapsed_time(evs[i + 1]) for i in range(reps)])) / per_graph
 
-    reps = max(1, args.roofline_iters // (4 * n_sets))
+    def time_single(fn, reps=50, warm=10):
+        """One launch at a time: events around it, a synchronize after each,
+        so launch latency is included (median)."""
+        out = []
+        for i in range(warm + reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn(sets[i % n_sets])
+            b.record()
+            torch.cuda.synchronize()
+            if i >= warm:
+                out.append(a.elapsed_time(b))
+        return float(np.median(out))
+
+    reps = max(50, args.roofline_iters // (4 * n_sets))
     t_fwd = time_launches(fwd, reps)
     t_bwd = time_launches(bwd, reps)
     t_sp2hp = time_launches(lambda s: ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype), reps)
+    single = {"fwd": time_single(fwd), "bwd": time_single(bwd),
+              "sp2hp": time_single(lambda s: ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype))}
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -351,7 +370,12 @@ def run_ours(args):
                 "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
                 "peak_source": peak_src, "algorithmic_bytes_per_launch": d_bytes,
                 "launch_ms": round(d_ms, 5),
-                "per_kernel": {k: {"launch_ms": round(v[0], 5), "algorithmic_bytes": v[1],
+                "launch_timing": "launch_ms: median over CUDA graph replays of back-to-back "
+                                 "launches over the rotating buffer sets; single_launch_ms: median "
+                                 "of 50 launches each alone between events and a synchronize "
+                                 "(includes launch latency)",
+                "per_kernel": {k: {"launch_ms": round(v[0], 5), "single_launch_ms": round(single[k], 5),
+                                   "algorithmic_bytes": v[1],
                                    "gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
                                    "frac_of_measured": round(v[1] / (v[0] / 1e3) / 1e9 / hbm_peak, 4),
                                    "frac_of_nominal_8000": round(v[1] / (v[0] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
@@ -406,15 +430,42 @@ def run_e2e(args, w, desc, dev, sets, rows, world):
     from residual_sp_rs_gb300 import ops
 
     T, H = w.T, w.H
-    dsets = sets[:2]
-    s0 = dsets[0]
-    host_in = {k: s0[k].cpu().pin_memory() for k in ("residual", "dy", "dh", "gamma")}
-    host_parts = [p.view(rows, H).cpu().pin_memory() for p in s0["partials"]]
-    outs = ("y", "d_res", "d_sum", "dgamma")
-    host_out = {k: torch.empty(s0[k].shape, dtype=s0[k].dtype, pin_memory=True) for k in outs}
-    bi = sum(v.numel() * v.element_size() for v in host_in.values()) + \
-        sum(v.numel() * v.element_size() for v in host_parts)
-    bo = sum(v.numel() * v.element_size() for v in host_out.values())
+    s0 = sets[0]
+
+    def packed(named, device, pin=False):
+        """One flat byte buffer holding tensors shaped like `named`, each at a
+        256-byte aligned offset; returns (flat, views)."""
+        offs, off = [], 0
+        for _, v in named:
+            offs.append(off)
+            off += -(-v.numel() * v.element_size() // 256) * 256
+        flat = torch.empty(off, dtype=torch.uint8, device=device, pin_memory=pin)
+        views = [flat[o:o + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+                 for o, (_, v) in zip(offs, named)]
+        return flat, views
+
+    # a step's inputs travel as one block and its results as another: one
+    # copy each way per step
+    in_named = [(f"P{t}", p.view(rows, H)) for t, p in enumerate(s0["partials"])]
+    in_named += [(k, s0[k]) for k in ("residual", "dy", "dh", "gamma", "beta") if s0[k] is not None]
+    out_named = [(k, s0[k]) for k in ("y", "d_res", "d_sum", "dgamma", "dbeta") if s0[k] is not None]
+    host_in, hv = packed(in_named, "cpu", pin=True)
+    for (_, v), h in zip(in_named, hv):
+        h.copy_(v.cpu())
+    host_out, _ = packed(out_named, "cpu", pin=True)
+    dsets, dev_in, dev_out = [], [], []
+    for k in range(2):
+        fi, vi = packed(in_named, dev)
+        fo, vo = packed(out_named, dev)
+        d = dict(sets[k])
+        d["partials"] = vi[:T]
+        d.update({name: v for (name, _), v in zip(in_named[T:], vi[T:])})
+        d.update({name: v for (name, _), v in zip(out_named, vo)})
+        dsets.append(d)
+        dev_in.append(fi)
+        dev_out.append(fo)
+    bi = host_in.numel()
+    bo = host_out.numel()
     st_in, st_cmp, st_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in dsets]
     ev_cmp = [torch.cuda.Event() for _ in dsets]
@@ -425,10 +476,7 @@ def run_e2e(args, w, desc, dev, sets, rows, world):
         s = dsets[k]
         st_in.wait_event(ev_cmp[k])  # the set's inputs are free once its last step ran
         with torch.cuda.stream(st_in):
-            for name, v in host_in.items():
-                s[name].copy_(v, non_blocking=True)
-            for p, hp in zip(s["partials"], host_parts):
-                p.view(rows, H).copy_(hp, non_blocking=True)
+            dev_in[k].copy_(host_in, non_blocking=True)
             ev_in[k].record(st_in)
         st_cmp.wait_event(ev_in[k])
         st_cmp.wait_event(ev_out[k])  # the set's outputs are free once copied out
@@ -443,8 +491,7 @@ def run_e2e(args, w, desc, dev, sets, rows, world):
             ev_cmp[k].record(st_cmp)
         st_out.wait_event(ev_cmp[k])
         with torch.cuda.stream(st_out):
-            for name in outs:
-                host_out[name].copy_(s[name], non_blocking=True)
+            host_out.copy_(dev_out[k], non_blocking=True)
             ev_out[k].record(st_out)
 
     for i in range(6):
@@ -460,7 +507,8 @@ def run_e2e(args, w, desc, dev, sets, rows, world):
     return {"value": round(rows * args.e2e_steps * world / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps,
             "ms_per_step": round(ms / args.e2e_steps, 5),
-            "pipeline": "copy-in / step / copy-out on three streams over two device buffer sets"}
+            "pipeline": "copy-in / step / copy-out on three streams over two device buffer sets; "
+                        "each step's inputs and results each one packed pinned block (one copy each way)"}
 
 
 # ---------------------------------------------------------------------------
@@ -498,7 +546,42 @@ def _oracle_step(oracle, w, st, row0, n):
                     f["mask"], w.dtype)
 
 
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+class _PinnedThread:
+    """Pins the calling thread to one core (the last one it may use) for the
+    oracle's timing, and restores its affinity afterwards."""
+
+    def __enter__(self):
+        self.saved = os.sched_getaffinity(0)
+        self.core = max(self.saved)
+        os.sched_setaffinity(0, {self.core})
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.saved)
+        return False
+
+
+def _host_note(core):
+    return f"single thread pinned to core {core}; host: {os.cpu_count()} cores, {_cpu_model()}"
+
+
 def cpu_baseline(w, seconds):
+    with _PinnedThread() as pin:
+        return _cpu_baseline(w, seconds, pin.core)
+
+
+def _cpu_baseline(w, seconds, core):
     oracle, st = _oracle_setup(w)
     rows = w.S * w.B
     n = max(w.T, (64 // w.T) * w.T)
@@ -512,7 +595,7 @@ def cpu_baseline(w, seconds):
     return {"value": round(done / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{done} token rows ({done / rows:.2f} of one step's {rows}) of the same "
                       f"workload through the fp64 oracle (fwd, sp2hp, hp2sp, bwd), {dt:.1f} s, "
-                      f"single thread; host has {os.cpu_count()} cores"}
+                      + _host_note(core)}
 
 
 def run_reference(args):
@@ -523,6 +606,11 @@ def run_reference(args):
     from residual_sp_rs_gb300 import synthetic as syn
 
     w = syn.WORKLOADS[args.workload]
+    with _PinnedThread() as pin:
+        _run_reference(args, world, w, pin.core)
+
+
+def _run_reference(args, world, w, core):
     oracle, st = _oracle_setup(w)
     rows = w.S * w.B
     # size each step's sample so the whole run ends within about two minutes
@@ -540,7 +628,7 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     value = n * args.steps / dt
     sample = (f"{n} of {rows} token rows per step through the fp64 oracle "
-              f"(fwd, sp2hp, hp2sp, bwd), single thread; host has {os.cpu_count()} cores")
+              f"(fwd, sp2hp, hp2sp, bwd), " + _host_note(core))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
