@@ -217,7 +217,10 @@ def run_ours(args):
 
     first = make_set(0)
     per_set = set_bytes(first)
-    n_sets = max(2, -(-2 * l2 // per_set) + 1)
+    # enough buffer sets that each kernel's own bytes over a rotation exceed
+    # twice the L2 (the layout kernel, touching only y and y_hp, needs most)
+    touched = min(fwd_bytes(w, rows), bwd_bytes(w, rows), layout_bytes(w, rows), per_set)
+    n_sets = max(2, -(-2 * l2 // touched) + 1)
     sets = [first] + [make_set(k) for k in range(1, n_sets)]
 
     def fwd(s, stream=None):
@@ -244,13 +247,20 @@ def run_ours(args):
         if join:
             cur.wait_stream(side)
 
-    def rotation():
-        # n_sets consecutive steps, step k on buffer set k; the layout branch
-        # of a step joins the main stream at the end of the rotation (no step
-        # in between touches its buffers)
-        for s in sets:
-            step(s, join=False)
-        torch.cuda.current_stream().wait_stream(side)
+    # a graph replay boundary costs a few microseconds (the next replay starts
+    # only when the previous one has finished, with no programmatic dependent
+    # launch across them): one graph holds enough rotations for about 64 steps
+    n_rot = max(1, -(-64 // n_sets))
+    steps_per_graph = n_rot * n_sets
+
+    def rotations():
+        # n_rot times n_sets consecutive steps, step k on buffer set k % n_sets;
+        # the layout branch of a step joins the main stream at the end of its
+        # rotation (no step in between touches its buffers)
+        for _ in range(n_rot):
+            for s in sets:
+                step(s, join=False)
+            torch.cuda.current_stream().wait_stream(side)
 
     for s in sets:
         step(s)
@@ -261,7 +271,7 @@ def run_ours(args):
     cap_stream = torch.cuda.Stream()
     g_rot = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_rot, stream=cap_stream, capture_error_mode="relaxed"):
-        rotation()
+        rotations()
     graphs = []
     for s in sets:
         g = torch.cuda.CUDAGraph()
@@ -271,10 +281,10 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     def run_steps(k):
-        for _ in range(k // n_sets):
+        for _ in range(k // steps_per_graph):
             g_rot.replay()
-        for i in range(k % n_sets):
-            graphs[i].replay()
+        for i in range(k % steps_per_graph):
+            graphs[i % n_sets].replay()
 
     run_steps(args.warmup)
     torch.cuda.synchronize()
@@ -303,7 +313,7 @@ def run_ours(args):
     # back to back from one CUDA graph over the rotating sets, CUDA events
     # around the replays on the launching stream
     def time_launches(fn, reps):
-        per_graph = 4 * n_sets
+        per_graph = steps_per_graph
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="relaxed"):
             for i in range(per_graph):
@@ -334,7 +344,7 @@ def run_ours(args):
                 out.append(a.elapsed_time(b))
         return float(np.median(out))
 
-    reps = max(50, args.roofline_iters // (4 * n_sets))
+    reps = max(50, args.roofline_iters // steps_per_graph)
     t_fwd = time_launches(fwd, reps)
     t_bwd = time_launches(bwd, reps)
     t_sp2hp = time_launches(lambda s: ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype), reps)
@@ -401,11 +411,12 @@ def run_ours(args):
                                    f"H={H} {w.dtype} {w.norm} p={w.p}",
                        "T": T, "S": w.S, "B": w.B, "H": H, "norm": w.norm, "p": w.p,
                        "tokens_per_step": rows, "parallelism": f"replica x{world}",
-                       "l2": f"inputs rotate over {n_sets} buffer sets, {n_sets * per_set / 1e6:.0f} MB "
-                             f"> 2x L2 ({l2 / 1e6:.0f} MB)",
-                       "launch": f"one CUDA graph replay per rotation of {n_sets} steps over the buffer "
-                                 "sets (layout branch concurrent with the backward), programmatic "
-                                 "dependent launch"},
+                       "l2": f"inputs rotate over {n_sets} buffer sets, {n_sets * per_set / 1e6:.0f} MB; "
+                             f"each kernel's own bytes over a rotation > 2x L2 ({l2 / 1e6:.0f} MB)",
+                       "launch": f"one CUDA graph replay per {steps_per_graph} steps ({n_rot} rotations "
+                                 f"over the {n_sets} buffer sets; layout branch concurrent with the "
+                                 "backward, joined once per rotation), programmatic dependent launch "
+                                 "between the kernels of a replay; single-step graphs for a remainder"},
             "hbm_gbs_step": round(step_gbs, 1),
             "hbm_frac_step": round(step_gbs / hbm_peak, 4),
             "hbm_frac_step_of_nominal_8000": round(step_gbs / NOMINAL_HBM_GBS, 4),
