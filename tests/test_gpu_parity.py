@@ -282,6 +282,9 @@ def test_bwd_large_hidden_sampled(p):
     (3, 12, 2, 1024, "bf16", "rms", 0.1), (4, 16, 2, 256, "bf16", "ln", 0.1),
     (2, 10, 3, 512, "bf16", "ln", 0.5), (3, 9, 2, 2064, "bf16", "rms", 0.1),
     (2, 8, 3, 2064, "bf16", "ln", 0.1),
+    # two 8-warp LayerNorm row groups in the 768-thread block, several rows
+    # per CTA: ragged last slot, and no dropout
+    (2, 128, 3, 2064, "bf16", "ln", 0.1), (2, 160, 2, 4096, "bf16", "ln", 0.0),
 ])
 def test_bwd_edge_shapes(case):
     T, S, B, H, dt, nm, p = case
