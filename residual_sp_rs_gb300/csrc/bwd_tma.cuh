@@ -47,7 +47,13 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
   extern __shared__ __align__(16) unsigned char dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
   uint64_t* empty = full + L.nst;
-  float* sgam = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // gamma [H] fp32
+  // gamma, fp32.  With KEEP as two planes of float4 -- elements 0..3 of every
+  // vector, then elements 4..7 -- so a warp's reads of consecutive vectors
+  // are contiguous (no bank conflicts); otherwise vector by vector, whose
+  // simpler addressing keeps the register-tight variants from spilling
+  // (measured faster there despite the conflicts).
+  constexpr bool kPlanar = KEEP;
+  float* sgam = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));
   unsigned char* stages = dsm + L.smem_stages;
 
   // kernel parameters used in the hot loop, held in registers
@@ -108,8 +114,8 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
     for (int i = threadIdx.x; i < nvec; i += nthr_cons) {
       float g[EV];
       Act16<__nv_bfloat16>::unpack(ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV), g);
-      reinterpret_cast<float4*>(sgam)[2 * i] = make_float4(g[0], g[1], g[2], g[3]);
-      reinterpret_cast<float4*>(sgam)[2 * i + 1] = make_float4(g[4], g[5], g[6], g[7]);
+      reinterpret_cast<float4*>(sgam)[kPlanar ? i : 2 * i] = make_float4(g[0], g[1], g[2], g[3]);
+      reinterpret_cast<float4*>(sgam)[kPlanar ? nvec + i : 2 * i + 1] = make_float4(g[4], g[5], g[6], g[7]);
     }
   }
   __syncthreads();
@@ -227,10 +233,11 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
         const int v = lr + k * tpr;
         if (k < VPT - 1 || last_in) {
           const uint4 wdy = sdy[v], wh = sh[v];
-          const float4* gp = reinterpret_cast<const float4*>(sgam + v * EV);
+          const float4* gp = kPlanar ? reinterpret_cast<const float4*>(sgam) + v
+                                     : reinterpret_cast<const float4*>(sgam + v * EV);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float4 g4 = gp[q >> 1];
+            const float4 g4 = kPlanar ? gp[(q >> 1) * nvec] : gp[q >> 1];
             const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
             const f2_t dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]);
             const f2_t hq = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]);
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
       for (int k = 0; k < VPT; ++k) {
         const int v = lr + k * tpr;
         if (k < VPT - 1 || last_in) {
-          const float4* gp = reinterpret_cast<const float4*>(sgam + v * EV);
+          const float4* gp = reinterpret_cast<const float4*>(sgam + v * EV);  // !KEEP only
           uint4 wdh = make_uint4(0u, 0u, 0u, 0u);
           if constexpr (DH) wdh = sdh[v];
           // the stored mask is applied to the packed bf16 output as byte

@@ -135,7 +135,10 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
   extern __shared__ __align__(16) unsigned char dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
   uint64_t* empty = full + L.nst;
-  float* sgb = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));  // gamma[H], beta[H]
+  // gamma then beta, fp32, each as two planes of float4 -- elements 0..3 of
+  // every vector, then elements 4..7 -- so a warp's reads of consecutive
+  // vectors are contiguous (no bank conflicts)
+  float* sgb = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));
   unsigned char* stages = dsm + L.smem_stages;
 
   const int H = a.H, nvec = a.nvec, tpr = a.tpr;
@@ -233,12 +236,12 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
       if (i < nvec) {
         float g[EV];
         Act16<__nv_bfloat16>::unpack(gw[u], g);
-        reinterpret_cast<float4*>(sgb + i * EV)[0] = make_float4(g[0], g[1], g[2], g[3]);
-        reinterpret_cast<float4*>(sgb + i * EV)[1] = make_float4(g[4], g[5], g[6], g[7]);
+        reinterpret_cast<float4*>(sgb)[i] = make_float4(g[0], g[1], g[2], g[3]);
+        reinterpret_cast<float4*>(sgb)[nvec + i] = make_float4(g[4], g[5], g[6], g[7]);
         if constexpr (LN) {
           Act16<__nv_bfloat16>::unpack(bw[u], g);
-          reinterpret_cast<float4*>(sgb + H + i * EV)[0] = make_float4(g[0], g[1], g[2], g[3]);
-          reinterpret_cast<float4*>(sgb + H + i * EV)[1] = make_float4(g[4], g[5], g[6], g[7]);
+          reinterpret_cast<float4*>(sgb + H)[i] = make_float4(g[0], g[1], g[2], g[3]);
+          reinterpret_cast<float4*>(sgb + H)[nvec + i] = make_float4(g[4], g[5], g[6], g[7]);
         }
       }
     }
@@ -414,14 +417,14 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
     for (int k = 0; k < VPT; ++k) {
       const int v = lr + k * tpr;
       if (k < VPT - 1 || last_in) {
-        const float4* gp = reinterpret_cast<const float4*>(sgb + v * EV);
+        const float4* gp = reinterpret_cast<const float4*>(sgb) + v;
         uint32_t yw[4];
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
-          const float4 g4 = gp[q2];
+          const float4 g4 = gp[q2 * nvec];
           const f2_t ga = f2(g4.x, g4.y), gb = f2(g4.z, g4.w);
           if constexpr (LN) {
-            const float4 b4 = reinterpret_cast<const float4*>(sgb + H + v * EV)[q2];
+            const float4 b4 = (reinterpret_cast<const float4*>(sgb + H) + v)[q2 * nvec];
             yw[2 * q2] = f2_to_bf2(f2_fma(ga, f2_mul(f2_sub(hf.get(k, 2 * q2), mu2), r2), f2(b4.x, b4.y)));
             yw[2 * q2 + 1] =
                 f2_to_bf2(f2_fma(gb, f2_mul(f2_sub(hf.get(k, 2 * q2 + 1), mu2), r2), f2(b4.z, b4.w)));
