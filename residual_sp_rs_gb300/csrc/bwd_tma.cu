@@ -16,9 +16,10 @@ constexpr size_t kMinCopy = 16384;
 
 // The narrowest row group (<= 4 vectors per thread, <= 2 for LayerNorm,
 // whose dbeta accumulators add registers); as many row groups as the block
-// allows (15 warps at 512 threads; the wide block when that leaves one row
-// group and VPT <= 3) but no more than the rows a CTA owns; stages of rb
-// rows, as many as fit next to gamma.
+// allows (15 warps at 512 threads; when that leaves one row group of 8 warps
+// and VPT <= 3, two in the 544-thread block, which re-reads dy and h from
+// shared memory in the second pass) but no more than the rows a CTA owns;
+// stages of rb rows, as many as fit next to gamma.
 // At the end the ring must hold every row group's column sums.
 bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, int64_t rows_per_cta,
                   BwdTmaPlan* p) {
@@ -38,8 +39,8 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
   // the narrow block keeps dy and xhat in registers between the passes,
   // which pays more than extra warps unless it leaves a single row group
   int nrg = groups(kBwdTmaNarrow);
-  if (vpt <= 3 && nrg < 2 && groups(kBwdTmaWide) > nrg)
-    nrg = groups(kBwdTmaWide);
+  if (vpt <= 3 && nrg < 2 && groups(kBwdTmaMid) > nrg)
+    nrg = groups(kBwdTmaMid);
   const int ns = ln ? 2 : 1;
   const uint32_t rowb = (uint32_t)H * 2;
   const size_t fixed_base = (size_t)H * 4;  // gamma, fp32
@@ -78,7 +79,7 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
       p->shape.tpr = tpr;
       p->shape.vpt = vpt;
       p->shape.block = nrg * tpr + 32;
-      p->nthr = p->shape.block <= kBwdTmaNarrow ? kBwdTmaNarrow : kBwdTmaWide;
+      p->nthr = p->shape.block <= kBwdTmaNarrow ? kBwdTmaNarrow : kBwdTmaMid;
       p->smem = L.smem_stages + (size_t)nst * L.stage_bytes;
       return true;
     }

@@ -10,9 +10,9 @@
 // "empty" mbarrier.  The loads of up to nst*rb rows are in flight at all
 // times, without holding them in registers, so the HBM pipe stays busy
 // through the row reductions and the stores.  With the 512-thread block dy
-// and xhat stay in registers between the two passes over a row; the wider
-// block (fewer registers, for many short rows) reads them from shared memory
-// again.  gamma sits in shared memory as fp32.
+// and xhat stay in registers between the two passes over a row; the
+// 544-thread block (two 8-warp row groups, fewer registers) reads them from
+// shared memory again.  gamma sits in shared memory as fp32.
 // dgamma/dbeta accumulate in registers per thread-owned column; at the end
 // the row groups' sums go to the idle ring, are added in row-group order and
 // written as one fp32 partial row per CTA, which sp_colsum_kernel reduces in
@@ -29,10 +29,11 @@
 namespace spf {
 
 constexpr int kBwdTmaNarrowBlock = 512;  // the 16-warp block (128 registers)
+constexpr int kBwdTmaMidBlock = 544;     // two 8-warp row groups + producer (96 registers)
 
 // NTHR = 512: at most 16 warps (15 consumer + 1 producer), so 128 registers
 // per thread fit every SM sub-partition's register file; a wider block
-// trades registers for warps (768 threads: 80 registers).  KEEP: dy and xhat stay in registers between the
+// trades registers for warps (544 threads: 96 registers).  KEEP: dy and xhat stay in registers between the
 // two passes (VPT <= 3, 512 threads); otherwise pass 2 reads them from
 // shared memory again.  MASK: the keep bits come from the stored mask;
 // REGEN: they are recomputed from the seed (no mask stored), before the
@@ -47,12 +48,16 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
   extern __shared__ __align__(16) unsigned char dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
   uint64_t* empty = full + L.nst;
-  // gamma, fp32.  With KEEP as two planes of float4 -- elements 0..3 of every
-  // vector, then elements 4..7 -- so a warp's reads of consecutive vectors
-  // are contiguous (no bank conflicts); otherwise vector by vector, whose
-  // simpler addressing keeps the register-tight variants from spilling
-  // (measured faster there despite the conflicts).
+  // gamma, fp32.  With KEEP as two planes of float4 -- elements 0..3 of
+  // every vector, then elements 4..7 -- so a warp's float4 reads for
+  // consecutive vectors hit distinct banks.  In the 544-thread block vector by
+  // vector with the two float4 halves of vector v swapped when bit 2 of v is
+  // set, which also covers all 32 banks per quarter warp with simpler
+  // addressing.  Otherwise plain
+  // vector by vector: the 4-vector 512-thread backward measured 0.4% slower
+  // with the swizzle despite its two-way conflicts.
   constexpr bool kPlanar = KEEP;
+  constexpr int kSwz = (!KEEP && NTHR == kBwdTmaMidBlock) ? 1 : 0;
   float* sgam = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));
   unsigned char* stages = dsm + L.smem_stages;
 
@@ -114,8 +119,10 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
     for (int i = threadIdx.x; i < nvec; i += nthr_cons) {
       float g[EV];
       Act16<__nv_bfloat16>::unpack(ld_cached(reinterpret_cast<const __nv_bfloat16*>(a.gamma) + i * EV), g);
-      reinterpret_cast<float4*>(sgam)[kPlanar ? i : 2 * i] = make_float4(g[0], g[1], g[2], g[3]);
-      reinterpret_cast<float4*>(sgam)[kPlanar ? nvec + i : 2 * i + 1] = make_float4(g[4], g[5], g[6], g[7]);
+      const int sw = (i >> 2) & kSwz;
+      reinterpret_cast<float4*>(sgam)[kPlanar ? i : 2 * i + sw] = make_float4(g[0], g[1], g[2], g[3]);
+      reinterpret_cast<float4*>(sgam)[kPlanar ? nvec + i : 2 * i + (sw ^ 1)] =
+          make_float4(g[4], g[5], g[6], g[7]);
     }
   }
   __syncthreads();
@@ -163,8 +170,8 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
     // row slot i, its stage j = i / rb, the stage's row ri = i % rb, ring
     // slot s = j % nst and phase parity (j / nst) & 1.  In the 512-thread
     // block rb divides nrg, so iteration jj is stage jj * (nrg / rb) + rg / rb
-    // and ri = rg % rb throughout, which keeps its register budget; the wide
-    // block keeps them incrementally.
+    // and ri = rg % rb throughout, which keeps its register budget; the
+    // 544-thread block keeps them incrementally.
     constexpr bool kStageMajor = NTHR <= kBwdTmaNarrowBlock;
     int ri = rg % rb, s = (rg / rb) % nst, par = ((rg / rb) / nst) & 1;
     for (int i = rg, jj = 0; i < nslot; i += nrg, ++jj) {
@@ -237,7 +244,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
                                      : reinterpret_cast<const float4*>(sgam + v * EV);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float4 g4 = kPlanar ? gp[(q >> 1) * nvec] : gp[q >> 1];
+            const float4 g4 = kPlanar ? gp[(q >> 1) * nvec] : gp[(q >> 1) ^ ((v >> 2) & kSwz)];
             const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
             const f2_t dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy)[q]);
             const f2_t hq = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh)[q]);
@@ -282,8 +289,8 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
           uint4 wdh = make_uint4(0u, 0u, 0u, 0u);
           if constexpr (DH) wdh = sdh[v];
           // the stored mask is applied to the packed bf16 output as byte
-          // masks in the 16-warp block; the wide block (fewer registers) and
-          // the regenerated mask use keep bits
+          // masks in the 16-warp block; the 544-thread block (fewer
+          // registers) and the regenerated mask use keep bits
           constexpr bool kByteMask = MASK && NTHR <= kBwdTmaNarrowBlock;
           uint32_t mk = 0xFFu;
           uint2 mbytes = make_uint2(0u, 0u);  // each mask byte as 0x00 / 0xFF
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
               g = gk[k][q];
               xh = xhk[k][q];
             } else {
-              const float4 g4 = gp[q >> 1];
+              const float4 g4 = gp[(q >> 1) ^ ((v >> 2) & kSwz)];
               const f2_t gm = (q & 1) ? f2(g4.z, g4.w) : f2(g4.x, g4.y);
               dy = bf2_to_f2(reinterpret_cast<const uint32_t*>(&wdy2)[q]);
               xh = f2_mul(f2_sub(bf2_to_f2(reinterpret_cast<const uint32_t*>(&wh2)[q]), mu2), r2);

@@ -1,6 +1,6 @@
 // bwd_tma_inst.cuh -- instances of the TMA-fed backward for one norm:
 // VPT (1..4 RMSNorm, 1..2 LayerNorm), dh_out present or not, mask mode, and
-// the two block sizes (the 1024-thread one for VPT <= 3).
+// the two block sizes (544 threads for VPT <= 3).
 #pragma once
 
 #include "bwd_tma.cuh"
@@ -42,8 +42,8 @@ template <bool LN>
 cudaError_t launch_bwd_tma_impl(const BwdArgs& a, const BwdTmaPlan& p, dim3 grid, cudaStream_t st) {
   const bool dh = a.dh != nullptr;
   const int mode = a.mask ? 1 : (a.regen ? 2 : 0);
-  const BwdTmaKernel k = p.nthr == kBwdTmaWide ? bwd_tma_kernel_m<LN, kBwdTmaWide>(p.shape.vpt, dh, mode)
-                                               : bwd_tma_kernel_m<LN, kBwdTmaNarrow>(p.shape.vpt, dh, mode);
+  const BwdTmaKernel k = p.nthr == kBwdTmaMid ? bwd_tma_kernel_m<LN, kBwdTmaMid>(p.shape.vpt, dh, mode)
+                                              : bwd_tma_kernel_m<LN, kBwdTmaNarrow>(p.shape.vpt, dh, mode);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
   if (e != cudaSuccess) return e;

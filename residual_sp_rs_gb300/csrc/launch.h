@@ -55,14 +55,15 @@ cudaError_t launch_colsum(const float* ws, int nparts, int H, bool ln, float* dg
 
 // TMA-fed backward (bf16, H % 16 == 0): shared-memory ring layout and shape.
 // Block sizes the TMA backward is compiled for: 15 consumer warps + producer
-// (128 registers), or 23 + producer (80 registers, up to 3 vectors a thread).
+// (128 registers), or two 8-warp row groups + producer (96 registers, up to
+// 3 vectors a thread) for rows of 256 threads.
 constexpr int kBwdTmaNarrow = 512;
-constexpr int kBwdTmaWide = 768;
+constexpr int kBwdTmaMid = 544;
 
 struct BwdTmaPlan {
   RowShape shape;
   size_t smem;
-  int nthr;  // kBwdTmaNarrow or kBwdTmaWide
+  int nthr;  // kBwdTmaNarrow or kBwdTmaMid
   BwdTmaLayout layout;
 };
 bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, int64_t rows_per_cta,

@@ -277,12 +277,12 @@ def test_bwd_large_hidden_sampled(p):
     (2, 4, 5, 8192, "f32", "ln", 0.1), (4, 8, 3, 12, "f32", "rms", 0.7), (7, 14, 1, 1032, "f32", "ln", 0.0),
     (2, 2000, 1, 768, "bf16", "rms", 0.1),
     # each shared-memory-ring variant: 1, 2, 4 vectors a thread; LayerNorm 1
-    # and 2; ragged last vector slot in the 16-warp and the wide block
+    # and 2; ragged last vector slot in the 16-warp and the 544-thread block
     (4, 24, 2, 256, "bf16", "rms", 0.1), (2, 16, 3, 512, "bf16", "rms", 0.25),
     (3, 12, 2, 1024, "bf16", "rms", 0.1), (4, 16, 2, 256, "bf16", "ln", 0.1),
     (2, 10, 3, 512, "bf16", "ln", 0.5), (3, 9, 2, 2064, "bf16", "rms", 0.1),
     (2, 8, 3, 2064, "bf16", "ln", 0.1),
-    # two 8-warp LayerNorm row groups in the 768-thread block, several rows
+    # two 8-warp LayerNorm row groups in the 544-thread block, several rows
     # per CTA: ragged last slot, and no dropout
     (2, 128, 3, 2064, "bf16", "ln", 0.1), (2, 160, 2, 4096, "bf16", "ln", 0.0),
 ])
