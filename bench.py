@@ -223,27 +223,29 @@ def run_ours(args):
     n_sets = max(2, -(-2 * l2 // touched) + 1)
     sets = [first] + [make_set(k) for k in range(1, n_sets)]
 
-    def fwd(s, stream=None):
+    def fwd(s, stream=None, mask_free=False):
         ops.sp_rs_dropout_residual_norm_fwd(desc, s["partials"], s["residual"], s["gamma"], s["beta"],
-                                            s["h"], s["y"], s["mask"], s["rstd"], s["mean"], stream)
+                                            s["h"], s["y"], None if mask_free else s["mask"], s["rstd"],
+                                            s["mean"], stream)
 
-    def bwd(s, stream=None):
-        ops.sp_rs_dropout_residual_norm_bwd(desc, s["dy"], s["dh"], s["h"], s["gamma"], s["mask"],
+    def bwd(s, stream=None, mask_free=False):
+        ops.sp_rs_dropout_residual_norm_bwd(desc, s["dy"], s["dh"], s["h"], s["gamma"],
+                                            None if mask_free else s["mask"],
                                             s["rstd"], s["mean"], s["d_res"], s["d_sum"], s["dgamma"],
                                             s["dbeta"], s["ws"], stream=stream)
 
     side = torch.cuda.Stream()
 
-    def step(s, join=True):
+    def step(s, join=True, mask_free=False):
         # the layout transforms of y and the backward both depend only on the
         # forward: they run as two concurrent branches of the step
-        fwd(s)
+        fwd(s, mask_free=mask_free)
         cur = torch.cuda.current_stream()
         side.wait_stream(cur)
         with torch.cuda.stream(side):
             ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype)
             ops.hp2sp(s["y_hp"], s["y_sp"], rows, H, T, w.dtype)
-        bwd(s)
+        bwd(s, mask_free=mask_free)
         if join:
             cur.wait_stream(side)
 
@@ -253,13 +255,13 @@ def run_ours(args):
     n_rot = max(1, -(-64 // n_sets))
     steps_per_graph = n_rot * n_sets
 
-    def rotations():
+    def rotations(mask_free=False):
         # n_rot times n_sets consecutive steps, step k on buffer set k % n_sets;
         # the layout branch of a step joins the main stream at the end of its
         # rotation (no step in between touches its buffers)
         for _ in range(n_rot):
             for s in sets:
-                step(s, join=False)
+                step(s, join=False, mask_free=mask_free)
             torch.cuda.current_stream().wait_stream(side)
 
     for s in sets:
@@ -308,6 +310,31 @@ def run_ours(args):
     value = weak_scaling_tokens_per_s(rows, args.steps, world, ms)
     step_bytes = fwd_bytes(w, rows) + bwd_bytes(w, rows) + 2 * layout_bytes(w, rows)
     step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
+
+    # ---- the mask-free mode (not the headline): the forward stores no mask and
+    # the backward draws the keep bits again -- 2 bytes per element less
+    # traffic, Philox twice
+    mask_free = None
+    if w.p > 0:
+        g_mf = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_mf, stream=cap_stream, capture_error_mode="relaxed"):
+            rotations(mask_free=True)
+        for _ in range(3):
+            g_mf.replay()
+        torch.cuda.synchronize()
+        reps_mf = max(5, min(args.steps, 20000) // steps_per_graph)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps_mf):
+            g_mf.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_mf = max_over_ranks(e0.elapsed_time(e1), world, dev) / (reps_mf * steps_per_graph)
+        mask_free = {"ms_per_step": round(ms_mf, 6),
+                     "value": round(weak_scaling_tokens_per_s(rows, 1, world, ms_mf), 1),
+                     "unit": "tokens/s", "steps": reps_mf * steps_per_graph,
+                     "note": "same step with the mask pointers NULL: the forward keeps no mask, the "
+                             "backward regenerates the keep bits from the seed"}
 
     # ---- per-launch durations of the main kernels: each kernel alone, launched
     # back to back from one CUDA graph over the rotating sets, CUDA events
@@ -422,7 +449,7 @@ def run_ours(args):
             "hbm_frac_step_of_nominal_8000": round(step_gbs / NOMINAL_HBM_GBS, 4),
             "roofline": roofline,
             "gpu_launches": LAUNCHES_PER_STEP * args.steps,
-            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "mask_free": mask_free,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
