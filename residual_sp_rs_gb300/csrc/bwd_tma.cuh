@@ -289,9 +289,8 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
           uint4 wdh = make_uint4(0u, 0u, 0u, 0u);
           if constexpr (DH) wdh = sdh[v];
           // the stored mask is applied to the packed bf16 output as byte
-          // masks in the 16-warp block; the 544-thread block (fewer
-          // registers) and the regenerated mask use keep bits
-          constexpr bool kByteMask = MASK && NTHR <= kBwdTmaNarrowBlock;
+          // masks; the regenerated mask uses keep bits
+          constexpr bool kByteMask = MASK && NTHR <= kBwdTmaMidBlock;
           uint32_t mk = 0xFFu;
           uint2 mbytes = make_uint2(0u, 0u);  // each mask byte as 0x00 / 0xFF
           if constexpr (kByteMask) {
