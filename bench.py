@@ -78,6 +78,31 @@ def layout_bytes(w, rows):
     return 2 * rows * w.H * e
 
 
+def rotation_sets(l2: int, per_set: int, *kernel_bytes: int) -> int:
+    """How many buffer sets the steps rotate over: enough that each kernel's
+    own bytes over one rotation exceed twice the L2 (the layout kernel,
+    touching only y and y_hp, needs the most), and at least 2."""
+    touched = min(per_set, *kernel_bytes)
+    return max(2, -(-2 * l2 // touched) + 1)
+
+
+def packed_block(named, device, pin=False):
+    """One flat byte buffer holding tensors shaped like the (name, tensor)
+    pairs in `named`, each at a 256-byte aligned offset; returns (flat, views).
+    The end-to-end pipeline moves a step's inputs and results as one such
+    block each way."""
+    import torch
+
+    offs, off = [], 0
+    for _, v in named:
+        offs.append(off)
+        off += -(-v.numel() * v.element_size() // 256) * 256
+    flat = torch.empty(off, dtype=torch.uint8, device=device, pin_memory=pin)
+    views = [flat[o:o + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+             for o, (_, v) in zip(offs, named)]
+    return flat, views
+
+
 # ---------------------------------------------------------------------------
 # multi-rank aggregation (one process per GPU, the same workload on each)
 # ---------------------------------------------------------------------------
@@ -217,10 +242,7 @@ def run_ours(args):
 
     first = make_set(0)
     per_set = set_bytes(first)
-    # enough buffer sets that each kernel's own bytes over a rotation exceed
-    # twice the L2 (the layout kernel, touching only y and y_hp, needs most)
-    touched = min(fwd_bytes(w, rows), bwd_bytes(w, rows), layout_bytes(w, rows), per_set)
-    n_sets = max(2, -(-2 * l2 // touched) + 1)
+    n_sets = rotation_sets(l2, per_set, fwd_bytes(w, rows), bwd_bytes(w, rows), layout_bytes(w, rows))
     sets = [first] + [make_set(k) for k in range(1, n_sets)]
 
     def fwd(s, stream=None, mask_free=False):
@@ -470,31 +492,19 @@ def run_e2e(args, w, desc, dev, sets, rows, world):
     T, H = w.T, w.H
     s0 = sets[0]
 
-    def packed(named, device, pin=False):
-        """One flat byte buffer holding tensors shaped like `named`, each at a
-        256-byte aligned offset; returns (flat, views)."""
-        offs, off = [], 0
-        for _, v in named:
-            offs.append(off)
-            off += -(-v.numel() * v.element_size() // 256) * 256
-        flat = torch.empty(off, dtype=torch.uint8, device=device, pin_memory=pin)
-        views = [flat[o:o + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
-                 for o, (_, v) in zip(offs, named)]
-        return flat, views
-
     # a step's inputs travel as one block and its results as another: one
     # copy each way per step
     in_named = [(f"P{t}", p.view(rows, H)) for t, p in enumerate(s0["partials"])]
     in_named += [(k, s0[k]) for k in ("residual", "dy", "dh", "gamma", "beta") if s0[k] is not None]
     out_named = [(k, s0[k]) for k in ("y", "d_res", "d_sum", "dgamma", "dbeta") if s0[k] is not None]
-    host_in, hv = packed(in_named, "cpu", pin=True)
+    host_in, hv = packed_block(in_named, "cpu", pin=True)
     for (_, v), h in zip(in_named, hv):
         h.copy_(v.cpu())
-    host_out, _ = packed(out_named, "cpu", pin=True)
+    host_out, _ = packed_block(out_named, "cpu", pin=True)
     dsets, dev_in, dev_out = [], [], []
     for k in range(2):
-        fi, vi = packed(in_named, dev)
-        fo, vo = packed(out_named, dev)
+        fi, vi = packed_block(in_named, dev)
+        fo, vo = packed_block(out_named, dev)
         d = dict(sets[k])
         d["partials"] = vi[:T]
         d.update({name: v for (name, _), v in zip(in_named[T:], vi[T:])})
