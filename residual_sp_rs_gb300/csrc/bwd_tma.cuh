@@ -32,12 +32,12 @@ constexpr int kBwdTmaNarrowBlock = 512;  // the 16-warp block (128 registers)
 constexpr int kBwdTmaMidBlock = 544;     // two 8-warp row groups + producer (96 registers)
 
 // NTHR = 512: at most 16 warps (15 consumer + 1 producer), so 128 registers
-// per thread fit every SM sub-partition's register file; a wider block
-// trades registers for warps (544 threads: 96 registers).  KEEP: dy and xhat stay in registers between the
-// two passes (VPT <= 3, 512 threads); otherwise pass 2 reads them from
-// shared memory again.  MASK: the keep bits come from the stored mask;
-// REGEN: they are recomputed from the seed (no mask stored), before the
-// row's data is waited for.
+// per thread fit every SM sub-partition's register file; the 544-thread
+// block trades registers for warps (96 registers).  KEEP: dy and xhat stay
+// in registers between the two passes (VPT <= 3, 512 threads); otherwise
+// pass 2 reads them from shared memory again.  MASK: the keep bits come
+// from the stored mask; REGEN: they are recomputed from the seed (no mask
+// stored), before the row's data is waited for.
 template <bool LN, int VPT, bool DH, bool MASK, bool REGEN, int NTHR>
 __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, const BwdTmaLayout L) {
   constexpr bool KEEP = VPT <= 3 && NTHR <= 512;
@@ -50,12 +50,12 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
   uint64_t* empty = full + L.nst;
   // gamma, fp32.  With KEEP as two planes of float4 -- elements 0..3 of
   // every vector, then elements 4..7 -- so a warp's float4 reads for
-  // consecutive vectors hit distinct banks.  In the 544-thread block vector by
-  // vector with the two float4 halves of vector v swapped when bit 2 of v is
-  // set, which also covers all 32 banks per quarter warp with simpler
-  // addressing.  Otherwise plain
-  // vector by vector: the 4-vector 512-thread backward measured 0.4% slower
-  // with the swizzle despite its two-way conflicts.
+  // consecutive vectors hit distinct banks.  In the 544-thread block vector
+  // by vector with the two float4 halves of vector v swapped when bit 2 of v
+  // is set, which also covers all 32 banks per quarter warp with simpler
+  // addressing.  Otherwise plain vector by vector: the 4-vector 512-thread
+  // backward measured 0.4% slower with the swizzle despite its two-way
+  // conflicts.
   constexpr bool kPlanar = KEEP;
   constexpr int kSwz = (!KEEP && NTHR == kBwdTmaMidBlock) ? 1 : 0;
   float* sgam = reinterpret_cast<float*>(dsm + 16 * ((2 * L.nst * 8 + 15) / 16));
