@@ -5,9 +5,12 @@ pages' benchmark shape (T=2, S=2048, B=2, H=768, bf16, RMSNorm, p=0.1):
   forward of every sequence shard (reduce-scatter's reduce, dropout, residual,
   RMSNorm) -> sp2hp of the norm output -> hp2sp back -> backward of every
   shard (norm, residual and dropout backward, dgamma).
-Steps run from CUDA graphs, one replay per rotation over the buffer sets
-(each step of a rotation on its own set); the sets total more than twice the
-L2 size, so HBM (not L2) serves the inputs.
+Steps run from CUDA graphs of about 64 steps (whole rotations over the
+buffer sets, each step of a rotation on its own set); there are enough sets
+that every kernel's own bytes over a rotation exceed twice the L2 size, so
+HBM (not L2) serves the inputs.  The JSON line also carries per-kernel
+launch times (back to back and single), the end-to-end number through host
+buffers, the mask-free step, the oracle's CPU rate and the clocks seen.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
