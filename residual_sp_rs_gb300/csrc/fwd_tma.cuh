@@ -109,28 +109,22 @@ __device__ __forceinline__ void residual_vec8_drop(const f2_t (&acc)[4], const f
   }
 }
 
-// FAST: p > 0 with 1/(1-p) not dyadic (the common case) -- no tie rule, no
-// runtime mode branches in the element loop.  Otherwise GENERIC.
-template <int VPT, bool PACK>
-struct HRow;
+// A thread's share of the stored h of its row, as fp32 pairs, for the norm's
+// two passes.
 template <int VPT>
-struct HRow<VPT, false> {
+struct HRow {
   f2_t v[VPT][4];
-  __device__ __forceinline__ void set(int k, int q, uint32_t, f2_t f) { v[k][q] = f; }
+  __device__ __forceinline__ void set(int k, int q, f2_t f) { v[k][q] = f; }
   __device__ __forceinline__ f2_t get(int k, int q) const { return v[k][q]; }
 };
-template <int VPT>
-struct HRow<VPT, true> {
-  uint32_t w[VPT][4];
-  __device__ __forceinline__ void set(int k, int q, uint32_t b, f2_t) { w[k][q] = b; }
-  __device__ __forceinline__ f2_t get(int k, int q) const { return bf2_to_f2(w[k][q]); }
-};
+
+// FAST: p > 0 with 1/(1-p) not dyadic (the common case) -- no tie rule, no
+// runtime mode branches in the element loop.  Otherwise GENERIC.
 
 template <int T, bool LN, int VPT, bool FAST, int NTHR, bool CH>
 __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, const FwdTmaLayout L) {
   constexpr int EV = 8;
   constexpr int NCH = CH ? VPT : 1;  // stages per row stage (CH: rb == 1)
-  constexpr bool kPackH = NTHR > 896;  // fewer than 72 registers: keep h as bf16 pairs
   __shared__ float red[2 * 32 * 2];
   extern __shared__ __align__(16) unsigned char dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm);
@@ -307,7 +301,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
     // ---- reduce, dropout, residual add; store h ----------------------------
     // h stays in registers for the norm: as fp32 pairs (or, under a tighter
     // register budget, as the stored bf16 pairs, unpacked again per use)
-    HRow<VPT, kPackH> hf;
+    HRow<VPT> hf;
     f2_t s2 = f2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -348,7 +342,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const f2_t hq = bf2_to_f2(hw[q]);
-            hf.set(k, q, hw[q], hq);
+            hf.set(k, q, hq);
             s2 = LN ? f2_add(s2, hq) : f2_fma(hq, hq, s2);
           }
         } else {
@@ -366,7 +360,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
           }
           hw[q] = nontie ? residual_bf2_drop(res, acc, shi, slo) : residual_bf2(res, acc, shi, slo);
           const f2_t hq = bf2_to_f2(hw[q]);
-          hf.set(k, q, hw[q], hq);
+          hf.set(k, q, hq);
           s2 = LN ? f2_add(s2, hq) : f2_fma(hq, hq, s2);
         }
         }
