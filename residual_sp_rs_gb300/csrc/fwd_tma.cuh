@@ -299,8 +299,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
     __nv_bfloat16* y_row = reinterpret_cast<__nv_bfloat16*>(a.y) + r * (int64_t)H;
 
     // ---- reduce, dropout, residual add; store h ----------------------------
-    // h stays in registers for the norm: as fp32 pairs (or, under a tighter
-    // register budget, as the stored bf16 pairs, unpacked again per use)
+    // h stays in registers for the norm, as fp32 pairs
     HRow<VPT> hf;
     f2_t s2 = f2(0.f, 0.f);
 #pragma unroll
