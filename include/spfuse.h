@@ -219,6 +219,40 @@ const char* sp_last_cuda_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t sp_version(void);
 
+/* The launch configuration of one TMA-fed kernel (all fields 0 when the
+ * register-resident kernel would run instead).  Sizes in bytes. */
+typedef struct sp_kernel_plan_t {
+  int32_t tma;            /* 1: TMA-fed kernel, 0: register-resident kernel */
+  int32_t block;          /* threads launched per CTA (row groups + producer warp) */
+  int32_t nthr;           /* block size the kernel's registers are budgeted for */
+  int32_t tpr;            /* threads per token row */
+  int32_t vpt;            /* 16-byte vectors of the row per thread */
+  int32_t row_groups;     /* rows a CTA works on at the same time */
+  int32_t rows_per_stage; /* rows per shared-memory ring stage (1 when chunked) */
+  int32_t stages;         /* ring stages */
+  int32_t chunked;        /* forward only: a stage holds one column chunk of a row */
+  int32_t reserved;
+  int64_t stage_bytes;    /* one ring stage, all inputs */
+  int64_t smem_bytes;     /* dynamic shared memory per CTA */
+  int64_t rows_per_cta;   /* contiguous token rows each CTA owns */
+  int64_t ctas;           /* grid size */
+} sp_kernel_plan_t;
+
+typedef struct sp_plan_info_t {
+  sp_kernel_plan_t fwd;
+  sp_kernel_plan_t bwd;
+} sp_plan_info_t;
+
+/* What sp_rs_dropout_residual_norm_fwd / _bwd would launch for `desc` on a
+ * device with `sms` multiprocessors and `smem_optin` bytes of opt-in shared
+ * memory per block (the two values the calls read from the current device),
+ * for a backward with or without dh_out and a stored mask.  Host arithmetic
+ * only: needs no GPU and launches nothing.  `out` is caller-owned.  Errors:
+ * the descriptor's, SP_ERR_INVALID_ARG for a NULL `out` or non-positive
+ * limits. */
+sp_status_t sp_plan_describe(const sp_rs_desc_t* desc, int32_t sms, int32_t smem_optin,
+                             int32_t has_dh, int32_t has_mask, sp_plan_info_t* out);
+
 #ifdef __cplusplus
 }
 #endif

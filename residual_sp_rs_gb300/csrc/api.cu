@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 
 #include "../../include/spfuse.h"
 #include "launch.h"
@@ -107,6 +108,26 @@ struct BwdPlan {
 // has_dh / has_mask only shape the TMA ring; the choice of kernel and the
 // workspace size are decided with both present, so the workspace query and
 // the call always agree.
+// The TMA-fed backward on a device with `sms` multiprocessors and `optin`
+// bytes of opt-in shared memory per block, when it applies (bf16 and a ring
+// that fits): one CTA per SM over contiguous rows, one partial row each.
+bool plan_bwd_tma_for(const Problem& pr, bool has_dh, bool has_mask, int sms, int optin, BwdPlan* pl) {
+  const bool ln = pr.norm == SP_LAYERNORM;
+  if (pr.dtype != SP_BF16) return false;
+  const int64_t ctas = pr.rows < sms ? (pr.rows > 0 ? pr.rows : 1) : sms;
+  const int64_t rpc = pr.rows > 0 ? (pr.rows + ctas - 1) / ctas : 1;
+  BwdTmaPlan probe;
+  if (!plan_bwd_tma(pr.H, ln, true, true, optin, rpc, &probe) ||
+      !plan_bwd_tma(pr.H, ln, has_dh, has_mask, optin, rpc, &pl->tp))
+    return false;
+  pl->tma = true;
+  pl->rows_per_cta = rpc;
+  pl->ctas = pr.rows > 0 ? (int)((pr.rows + pl->rows_per_cta - 1) / pl->rows_per_cta) : 0;
+  pl->nparts = pl->ctas;
+  pl->ws_bytes = (size_t)(ctas > 0 ? ctas : 1) * (size_t)pr.H * sizeof(float) * (ln ? 2 : 1);
+  return true;
+}
+
 sp_status_t plan_bwd(const Problem& pr, bool has_dh, bool has_mask, BwdPlan* pl) {
   const bool ln = pr.norm == SP_LAYERNORM;
   pl->tma = false;
@@ -117,19 +138,9 @@ sp_status_t plan_bwd(const Problem& pr, bool has_dh, bool has_mask, BwdPlan* pl)
     if (qe == cudaSuccess)
       qe = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (qe != cudaSuccess) return from_cuda(qe);
-    const int64_t ctas = pr.rows < sms ? (pr.rows > 0 ? pr.rows : 1) : sms;
-    const int64_t rpc = pr.rows > 0 ? (pr.rows + ctas - 1) / ctas : 1;
-    BwdTmaPlan probe;
-    if (plan_bwd_tma(pr.H, ln, true, true, optin, rpc, &probe) &&
-        plan_bwd_tma(pr.H, ln, has_dh, has_mask, optin, rpc, &pl->tp)) {
-      pl->tma = true;
-      pl->rows_per_cta = rpc;
-      pl->ctas = pr.rows > 0 ? (int)((pr.rows + pl->rows_per_cta - 1) / pl->rows_per_cta) : 0;
-      pl->nparts = pl->ctas;
-      pl->ws_bytes = (size_t)(ctas > 0 ? ctas : 1) * (size_t)pr.H * sizeof(float) * (ln ? 2 : 1);
-      return SP_OK;
-    }
+    if (plan_bwd_tma_for(pr, has_dh, has_mask, sms, optin, pl)) return SP_OK;
   }
+  pl->tma = false;
   pl->shape = bwd_row_shape(pr);
   // CTA column sums, then the gamma vectors
   pl->smem = (size_t)(ln ? 2 : 1) * (size_t)pr.H * sizeof(float) + (size_t)pr.nvec * 16;
@@ -355,7 +366,52 @@ const char* sp_status_string(sp_status_t s) {
   }
 }
 
-int32_t sp_version(void) { return 100; }
+int32_t sp_version(void) { return 200; }
+
+sp_status_t sp_plan_describe(const sp_rs_desc_t* desc, int32_t sms, int32_t smem_optin,
+                             int32_t has_dh, int32_t has_mask, sp_plan_info_t* out) {
+  Problem pr;
+  sp_status_t st = check_desc(desc, &pr);
+  if (st != SP_OK) return st;
+  if (!out || sms < 1 || smem_optin < 1) return SP_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  if (pr.dtype != SP_BF16) return SP_OK;  // f32 runs the register-resident kernels
+  const bool ln = pr.norm == SP_LAYERNORM;
+  FwdTmaPlan tp;
+  if (plan_fwd_tma(pr.H, pr.T, ln, smem_optin, pr.rows, sms, &tp)) {
+    sp_kernel_plan_t& f = out->fwd;
+    f.tma = 1;
+    f.block = tp.shape.block;
+    f.nthr = tp.nthr;
+    f.tpr = tp.shape.tpr;
+    f.vpt = tp.shape.vpt;
+    f.row_groups = tp.layout.nrg;
+    f.rows_per_stage = tp.layout.rb;
+    f.stages = tp.layout.nst;
+    f.chunked = tp.chunked ? 1 : 0;
+    f.stage_bytes = tp.layout.stage_bytes;
+    f.smem_bytes = (int64_t)tp.smem;
+    f.rows_per_cta = tp.layout.rows_per_cta;
+    f.ctas = (pr.rows + tp.layout.rows_per_cta - 1) / tp.layout.rows_per_cta;
+  }
+  BwdPlan bp;
+  if (plan_bwd_tma_for(pr, has_dh != 0, has_mask != 0, sms, smem_optin, &bp)) {
+    sp_kernel_plan_t& b = out->bwd;
+    b.tma = 1;
+    b.block = bp.tp.shape.block;
+    b.nthr = bp.tp.nthr;
+    b.tpr = bp.tp.shape.tpr;
+    b.vpt = bp.tp.shape.vpt;
+    b.row_groups = bp.tp.layout.nrg;
+    b.rows_per_stage = bp.tp.layout.rb;
+    b.stages = bp.tp.layout.nst;
+    b.stage_bytes = bp.tp.layout.stage_bytes;
+    b.smem_bytes = (int64_t)bp.tp.smem;
+    b.rows_per_cta = bp.rows_per_cta;
+    b.ctas = bp.ctas;
+  }
+  return SP_OK;
+}
 
 const char* sp_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 

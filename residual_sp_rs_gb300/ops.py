@@ -44,6 +44,18 @@ class SpRsDesc(ctypes.Structure):
         return self.R * max(1, self.nshards)
 
 
+class SpKernelPlan(ctypes.Structure):
+    """Mirror of sp_kernel_plan_t (include/spfuse.h)."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("tma", "block", "nthr", "tpr", "vpt", "row_groups",
+                                              "rows_per_stage", "stages", "chunked", "reserved")] + \
+               [(n, ctypes.c_int64) for n in ("stage_bytes", "smem_bytes", "rows_per_cta", "ctas")]
+
+
+class SpPlanInfo(ctypes.Structure):
+    """Mirror of sp_plan_info_t (include/spfuse.h)."""
+    _fields_ = [("fwd", SpKernelPlan), ("bwd", SpKernelPlan)]
+
+
 def make_desc(T, j, S, B, H, dtype="bf16", norm="rms", p=0.0, eps=1e-6, seed=0, nshards=1):
     return SpRsDesc(T=T, j=j, S=S, B=B, H=H, dtype=NAME_CODE.get(dtype, dtype),
                     norm=NORM_CODE.get(norm, norm), p=p, eps=eps, seed=int(seed) & (2**64 - 1),
@@ -81,6 +93,8 @@ def lib() -> ctypes.CDLL:
         L.sp_version.argtypes = []
         L.sp_last_cuda_error.restype = ctypes.c_char_p
         L.sp_last_cuda_error.argtypes = []
+        L.sp_plan_describe.restype = ctypes.c_int
+        L.sp_plan_describe.argtypes = [D, i32, i32, i32, i32, ctypes.POINTER(SpPlanInfo)]
         _lib = L
     return _lib
 
@@ -107,6 +121,22 @@ def _check(code: int):
         if code == 6:  # SP_ERR_CUDA
             msg += f" ({lib().sp_last_cuda_error().decode()})"
         raise RuntimeError(msg)
+
+
+def sp_plan_describe(desc: SpRsDesc, sms: int, smem_optin: int, has_dh: bool = True,
+                     has_mask: bool = True) -> dict:
+    """The launch configurations the forward and backward would use on a device
+    with `sms` multiprocessors and `smem_optin` bytes of opt-in shared memory
+    per block; host arithmetic only (no GPU needed).  Returns
+    {"fwd": {...}, "bwd": {...}} with the fields of sp_kernel_plan_t."""
+    info = SpPlanInfo()
+    _check(lib().sp_plan_describe(ctypes.byref(desc), int(sms), int(smem_optin), int(bool(has_dh)),
+                                  int(bool(has_mask)), ctypes.byref(info)))
+    out = {}
+    for k in ("fwd", "bwd"):
+        kp = getattr(info, k)
+        out[k] = {n: getattr(kp, n) for n, _ in SpKernelPlan._fields_ if n != "reserved"}
+    return out
 
 
 def status_string(code: int) -> str:
