@@ -70,7 +70,8 @@ def _full_fwd_check(w, inp, j, nshards=1, p=None, seed=None):
         g["mask"] = np.ones_like(orc["mask"])
     if g["mean"] is None:
         g["mean"] = np.zeros(len(orc["rstd"]))
-    parity.compare_fwd(w.dtype, w.norm, g, orc, oracle.to_f64(_np(inp["gamma"]), w.dtype))
+    parity.compare_fwd(w.dtype, w.norm, g, orc, pr, _np(inp["gamma"]),
+                       None if inp["beta"] is None else _np(inp["beta"]))
     return out, orc
 
 
@@ -128,14 +129,14 @@ def test_fwd_large_hidden_every_shard_sampled(p):
         grows = j * R + rows
         idx = torch.from_numpy(grows).to(DEV)
         prows = [_np(fp.index_select(0, idx)) for fp in flat_parts]
-        orc = oracle.fwd_rows(_oracle_problem(w, j), grows, prows, _np(flat_res.index_select(0, idx)),
-                              gam, None, w.dtype)
+        pr = _oracle_problem(w, j)
+        orc = oracle.fwd_rows(pr, grows, prows, _np(flat_res.index_select(0, idx)), gam, None, w.dtype)
         ridx = torch.from_numpy(rows).to(DEV)
         g = dict(h=_np(out["h"].index_select(0, ridx)), y=_np(out["y"].index_select(0, ridx)),
                  mask=(_np(out["mask"].index_select(0, ridx)) if out["mask"] is not None
                        else np.ones((len(rows), H), np.uint8)),
                  rstd=_np(out["rstd"][ridx]), mean=np.zeros(len(rows)))
-        parity.compare_fwd(w.dtype, w.norm, g, orc, oracle.to_f64(gam, w.dtype))
+        parity.compare_fwd(w.dtype, w.norm, g, orc, pr, gam)
         del out
 
 
@@ -179,7 +180,7 @@ def test_fwd_p0_without_mask_is_exact_residual_add():
     g = _host(out)
     g["mask"] = np.ones_like(orc["mask"])
     g["mean"] = np.zeros(R)
-    parity.compare_fwd("bf16", "rms", g, orc, oracle.to_f64(_np(inp["gamma"]), "bf16"))
+    parity.compare_fwd("bf16", "rms", g, orc, pr, _np(inp["gamma"]))
 
 
 def test_fwd_empty_rows_is_a_no_op():
@@ -241,6 +242,20 @@ def test_bwd_parity(name, j, nshards, with_dh):
                orc_f["mask"], out)
 
 
+def test_bwd_gpt_layernorm_every_shard():
+    """GPT-style LayerNorm (T=8, 512 token rows per shard): the backward of
+    each single shard j = 0..7, with dgamma/dbeta over that shard's rows."""
+    w = syn.WORKLOADS["gpt_ln_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    for j in range(w.T):
+        pr, orc_f, saved, dy, dh = _bwd_inputs_from_oracle_fwd(w, j, 1, inp, grads)
+        out = ops.backward(_desc(w, j), dy, dh, saved["h"], inp["gamma"], saved["mask"], saved["rstd"],
+                           saved["mean"])
+        torch.cuda.synchronize()
+        _check_bwd(w, pr, orc_f["h"], _np(dy), _np(dh), _np(inp["gamma"]), orc_f["mask"], out)
+
+
 @pytest.mark.parametrize("p", [0.1, 0.0])
 def test_bwd_large_hidden_sampled(p):
     w = syn.WORKLOADS["large_rms_bf16"].with_(p=p)
@@ -248,7 +263,7 @@ def test_bwd_large_hidden_sampled(p):
     grads = syn.upstream_grads(w, DEV)
     gam = syn.fwd_inputs(w.with_(T=1, S=1, B=1), DEV)["gamma"]   # gamma only
     R, H = w.R, w.H
-    for j in [0, 5, 7]:
+    for j in range(w.T):   # every shard, in sequence
         sl = slice(j * R, (j + 1) * R)
         h = saved["h"].view(-1, H)[sl]
         pr = _oracle_problem(w, j, p=p)

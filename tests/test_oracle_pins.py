@@ -550,6 +550,108 @@ def test_backward_rows_match_full_backward():
         assert np.array_equal(full[k], rows[k]), k
 
 
+def _fwd_case(dtype, norm, seed):
+    """Shard-sized inputs in storage form: T=4, S=16, B=3, H=40 (12 rows per
+    shard), p = 0.25, LayerNorm beta when asked."""
+    rng = np.random.default_rng(seed)
+    T, S, B, H = 4, 16, 3, 40
+    st = np.float32 if dtype == "f32" else None
+
+    def draw(a):
+        return a.astype(np.float32) if st else oracle.bf16_from_f64(a)
+
+    parts = [draw(rng.standard_normal((S * B, H)) * 0.5) for _ in range(T)]
+    res = draw(rng.standard_normal((S * B, H)))
+    gam = draw(rng.uniform(0.5, 1.5, H))
+    bet = draw(rng.standard_normal(H) * 0.1) if norm == "ln" else None
+    return T, S, B, H, parts, res, gam, bet
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("norm", ["rms", "ln"])
+def test_forward_rows_match_full_forward(dtype, norm):
+    """The row-sampling forward (caller-given global row indices) equals the
+    matching rows of the full forward over every shard: contiguous, scattered
+    and reversed row sets inside each shard and across shards."""
+    T, S, B, H, parts, res, gam, bet = _fwd_case(dtype, norm, 31)
+    R = (S // T) * B
+    p = float(np.float32(0.25))
+    full = oracle.fwd(oracle.problem(T, 0, S, B, H, dtype, norm, p, 1e-5, 0x0123456789ABCDEF, nshards=T),
+                      parts, res, gam, bet, dtype)
+    sets = [np.arange(R), np.array([0, 5, 2, R - 1]), np.arange(R)[::-1]]
+    for j in range(T):
+        pr = oracle.problem(T, j, S, B, H, dtype, norm, p, 1e-5, 0x0123456789ABCDEF)
+        for local in sets:
+            grows = j * R + local
+            got = oracle.fwd_rows(pr, grows, [q[grows] for q in parts], res[grows], gam, bet, dtype)
+            for k in ["h", "y", "mask", "rstd", "mean", "h_exact", "y_exact"]:
+                assert np.array_equal(got[k], full[k][grows]), (j, k)
+    across = np.array([S * B - 1, 0, R, 3 * R + 1, R - 1])
+    pr = oracle.problem(T, 0, S, B, H, dtype, norm, p, 1e-5, 0x0123456789ABCDEF)
+    got = oracle.fwd_rows(pr, across, [q[across] for q in parts], res[across], gam, bet, dtype)
+    for k in ["h", "y", "mask", "rstd", "mean"]:
+        assert np.array_equal(got[k], full[k][across]), k
+    # a slip of the row index moves the mask to another row's generator words
+    slipped = oracle.fwd_rows(pr, across + 1, [q[across] for q in parts], res[across], gam, bet, dtype)
+    assert not np.array_equal(slipped["mask"], full["mask"][across])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("norm", ["rms", "ln"])
+def test_norm_stats_match_forward_and_library_moments(dtype, norm):
+    """Row statistics of stored rows equal the forward's own rstd/mean on the
+    same stored h, and torch's f64 moments: population variance (LayerNorm)
+    or mean square (RMSNorm, as the squared 2-norm over H)."""
+    T, S, B, H, parts, res, gam, bet = _fwd_case(dtype, norm, 32)
+    eps = 1e-5
+    pr = oracle.problem(T, 0, S, B, H, dtype, norm, float(np.float32(0.25)), eps, 7, nshards=T)
+    full = oracle.fwd(pr, parts, res, gam, bet, dtype)
+    rstd, mean = oracle.norm_stats(pr, full["h"], dtype)
+    assert np.array_equal(rstd, full["rstd"])
+    h = torch.from_numpy(oracle.to_f64(full["h"], dtype))
+    if norm == "ln":
+        assert np.array_equal(mean, full["mean"])
+        var, mu = torch.var_mean(h, dim=-1, correction=0)
+        np.testing.assert_allclose(mean, mu.numpy(), rtol=1e-13, atol=1e-15)
+    else:
+        assert np.all(mean == 0.0)
+        var = torch.linalg.vector_norm(h, dim=-1) ** 2 / H
+    np.testing.assert_allclose(rstd, 1.0 / np.sqrt(var.numpy() + eps), rtol=1e-13)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("norm", ["rms", "ln"])
+def test_norm_of_stored_rows_is_the_norm_of_the_given_rows(dtype, norm):
+    """The parity rule's re-evaluation of the norm on another stored h: on the
+    forward's own h it reproduces the forward bit for bit; on a row with one
+    element moved by one unit in the last place it equals torch's f64 norm of
+    that row, and only that row changes."""
+    from tests import parity
+
+    T, S, B, H, parts, res, gam, bet = _fwd_case(dtype, norm, 33)
+    eps = 1e-5
+    pr = oracle.problem(T, 0, S, B, H, dtype, norm, float(np.float32(0.25)), eps, 7, nshards=T)
+    full = oracle.fwd(pr, parts, res, gam, bet, dtype)
+    same = parity.norm_of_stored_rows(pr, full["h"], gam, bet, dtype)
+    for k in ["y", "y_exact", "rstd", "mean"]:
+        assert np.array_equal(same[k], full[k]), k
+    h2 = full["h"].copy()
+    if dtype == "bf16":
+        h2[3, 5] = h2[3, 5] + np.uint16(1)
+    else:
+        h2[3, 5] = np.nextafter(h2[3, 5], np.float32(np.inf))
+    moved = parity.norm_of_stored_rows(pr, h2, gam, bet, dtype)
+    changed = np.flatnonzero((moved["y_exact"] != full["y_exact"]).any(-1))
+    assert list(changed) == [3]
+    x = torch.from_numpy(oracle.to_f64(h2[3:4], dtype))
+    g = torch.from_numpy(oracle.to_f64(gam, dtype))
+    if norm == "ln":
+        ref = torch.nn.functional.layer_norm(x, (H,), g, torch.from_numpy(oracle.to_f64(bet, dtype)), eps)
+    else:
+        ref = torch.nn.functional.rms_norm(x, (H,), g, eps)
+    np.testing.assert_allclose(moved["y_exact"][3:4], ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
 # ---------------------------------------------------------------------------
 # a8/a9: sp2hp / hp2sp (LLM Infra Atlas "03 · Sequence Parallelism", §5)
 # ---------------------------------------------------------------------------
