@@ -3,29 +3,39 @@
 One step = one pass of the whole hot path over one synthetic batch of the
 pages' benchmark shape (T=2, S=2048, B=2, H=768, bf16, RMSNorm, p=0.1):
   forward of every sequence shard (reduce-scatter's reduce, dropout, residual,
-  RMSNorm) -> sp2hp of the norm output -> hp2sp back -> backward of every
-  shard (norm, residual and dropout backward, dgamma).
-Steps run from CUDA graphs of about 64 steps (whole rotations over the
-buffer sets, each step of a rotation on its own set); there are enough sets
-that every kernel's own bytes over a rotation exceed twice the L2 size, so
-HBM (not L2) serves the inputs.  The JSON line also carries per-kernel
-launch times (back to back and single), the end-to-end number through host
-buffers, the mask-free step, the oracle's CPU rate and the clocks seen.
+  RMSNorm) -> sp2hp of the norm output -> hp2sp back (on a side stream,
+  concurrent with) the backward of every shard (norm, residual and dropout
+  backward, dgamma).
+The timed run is exactly --steps steps, replayed from CUDA graphs of (at
+most 512) consecutive steps, each step on its own buffer set; the sets rotate
+so that between two uses of a set every kernel's own bytes exceed twice the
+L2, so HBM (not L2) serves the inputs.  The timed run is repeated until the
+runs cover at least 50 ms (and at least 3 runs); the reported time is the
+median run.  The JSON line also carries per-kernel launch times (back to back
+and single), the end-to-end number through host buffers, the mask-free step,
+the oracle's CPU rate, the clocks seen, and the same per-kernel figures for
+the other workloads (GPT LayerNorm, the large-hidden stress case at p = 0.1
+and p = 0, and the layout transforms) under "workloads".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Rank 0 prints one JSON line.  Under torchrun every rank runs the same
-workload on its own GPU (weak scaling; no data-path collective).
+Rank 0 prints one JSON line.  Under torchrun rank r plays tensor-parallel
+rank r % T of data-parallel replica r // T: it runs its own sequence shard
+(forward, layout, backward of shard j = r % T) of its replica's batch, with
+no data-path collective (weak scaling once N >= T; one GPU alone plays the
+whole tensor-parallel group and runs every shard).
 """
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import platform
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -38,13 +48,19 @@ WORKLOAD = "pages_rms_bf16"
 METRIC = "SP-region fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 LAUNCHES_PER_STEP = 5  # fwd, sp2hp, hp2sp, bwd, dgamma column sum
 NOMINAL_HBM_GBS = 8000.0  # GB300's nominal HBM3e bandwidth (the measured copy peak is the roofline)
+MAX_GRAPH_STEPS = 512
+MIN_TIMED_MS = 50.0
+# the other workloads reported beside the headline: (key, workload, p override)
+EXTRA_WORKLOADS = [("gpt_ln_bf16", "gpt_ln_bf16", None),
+                   ("large_rms_bf16_p0.1", "large_rms_bf16", 0.1),
+                   ("large_rms_bf16_p0", "large_rms_bf16", 0.0)]
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--roofline-iters", type=int, default=400)
@@ -53,6 +69,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--seq", type=int, default=None,
                     help="override S (smaller captures of the same kernels for ncu)")
     return ap.parse_args()
@@ -89,6 +106,48 @@ def rotation_sets(l2: int, per_set: int, *kernel_bytes: int) -> int:
     return max(2, -(-2 * l2 // touched) + 1)
 
 
+def graph_steps(steps: int) -> int:
+    """Steps per CUDA graph for a timed run of `steps` steps: all of them up
+    to MAX_GRAPH_STEPS, else the largest divisor of `steps` not above it."""
+    if steps <= MAX_GRAPH_STEPS:
+        return steps
+    d = max(k for k in range(1, MAX_GRAPH_STEPS + 1) if steps % k == 0)
+    if d < 16:
+        raise ValueError(f"--steps {steps} has no divisor in [16, {MAX_GRAPH_STEPS}]; pick another count")
+    return d
+
+
+def graph_rotation(g: int, min_sets: int) -> tuple[int, int]:
+    """(buffer sets, graph variants) for graphs of g consecutive steps that
+    continue one rotation over the sets from replay to replay: at least
+    min_sets sets; a multiple of g when g is smaller (variant v starts at set
+    v*g), else a divisor of g (every graph starts at set 0)."""
+    if g < min_sets:
+        n = -(-min_sets // g) * g
+        return n, n // g
+    n = min(k for k in range(min_sets, g + 1) if g % k == 0)
+    return n, 1
+
+
+def timed_runs(run_once, min_ms: float = MIN_TIMED_MS, min_runs: int = 3, max_runs: int = 1000):
+    """Repeat run_once() (which returns its own duration in ms) until the runs
+    cover min_ms and there are at least min_runs; returns the durations."""
+    out = []
+    while len(out) < min_runs or (sum(out) < min_ms and len(out) < max_runs):
+        out.append(run_once())
+    return out
+
+
+def tp_dp_rank(rank: int, world: int, T: int) -> tuple[int, int, int]:
+    """(first shard j, shards in this rank's call, data-parallel replica) of
+    a rank: one GPU alone plays the whole tensor-parallel group (all T
+    shards); with N ranks, rank r is tensor-parallel rank r % T of replica
+    r // T and owns sequence shard r % T."""
+    if world <= 1:
+        return 0, T, 0
+    return rank % T, 1, rank // T
+
+
 def packed_block(named, device, pin=False):
     """One flat byte buffer holding tensors shaped like the (name, tensor)
     pairs in `named`, each at a 256-byte aligned offset; returns (flat, views).
@@ -107,7 +166,7 @@ def packed_block(named, device, pin=False):
 
 
 # ---------------------------------------------------------------------------
-# multi-rank aggregation (one process per GPU, the same workload on each)
+# multi-rank aggregation (one process per GPU)
 # ---------------------------------------------------------------------------
 
 def max_over_ranks(ms: float, world: int, device) -> float:
@@ -123,7 +182,7 @@ def max_over_ranks(ms: float, world: int, device) -> float:
 
 def weak_scaling_tokens_per_s(tokens_per_step: int, steps: int, world: int, ms: float) -> float:
     """Whole-job throughput: every rank processed `steps` steps of its own
-    batch in at most `ms` milliseconds."""
+    `tokens_per_step` token rows in at most `ms` milliseconds."""
     return tokens_per_step * steps * world / (ms / 1e3)
 
 
@@ -139,11 +198,11 @@ class ClockSampler:
     def __init__(self, device_index, enabled=True):
         self.proc = None
         self.idx = device_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
         if enabled:
             try:
-                os.makedirs(os.path.dirname(self.path), exist_ok=True)
-                self.f = open(self.path, "w")
+                self.f = tempfile.NamedTemporaryFile("w+", prefix=f"spfuse_clocks{device_index}_",
+                                                     suffix=".csv", delete=False)
+                self.path = self.f.name
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.FIELDS}",
                      "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
@@ -162,7 +221,10 @@ class ClockSampler:
             self.proc.kill()
         self.f.close()
         rows = []
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        os.unlink(self.path)
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -189,6 +251,236 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
+class Harness:
+    """Buffer sets, launch wrappers and graph timing for one workload on one
+    rank: shards j .. j+nshards-1 of the workload's batch."""
+
+    def __init__(self, w, dev, j, nshards, seed_offset=0, sets_for=None):
+        import torch
+
+        from residual_sp_rs_gb300 import ops, synthetic as syn
+
+        self.torch, self.ops, self.syn = torch, ops, syn
+        self.w, self.dev = w, dev
+        self.T, self.H = w.T, w.H
+        self.rows = w.R * nshards
+        self.row0 = w.R * j
+        self.desc = ops.make_desc(w.T, j, w.S, w.B, w.H, w.dtype, w.norm, w.p, w.eps, w.seed + seed_offset,
+                                  nshards=nshards)
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.seed_offset = seed_offset
+        first = self.make_set(0)
+        self.per_set = self.set_bytes(first)
+        need = rotation_sets(self.l2, self.per_set, fwd_bytes(w, self.rows), bwd_bytes(w, self.rows),
+                             layout_bytes(w, self.rows))
+        # sets_for: the caller's set count for this need (e.g. to suit its graphs)
+        self.n_sets = sets_for(need) if sets_for else need
+        self.sets = [first] + [self.make_set(k) for k in range(1, self.n_sets)]
+        self.side = torch.cuda.Stream()
+        self.cap_stream = torch.cuda.Stream()
+
+    def make_set(self, k):
+        torch, syn, w = self.torch, self.syn, self.w
+        seed = w.input_seed + 17 * k + 1000 * self.seed_offset
+        inp = syn.fwd_inputs(w, self.dev, seed=seed)
+        gr = syn.upstream_grads(w, self.dev, seed=seed)
+        rows, H, r0 = self.rows, self.H, self.row0
+        tdt = syn.torch_dtype(w.dtype)
+        s = dict(partials=inp["partials"], residual=inp["residual"].view(-1, H)[r0:r0 + rows],
+                 gamma=inp["gamma"], beta=inp["beta"], dy=gr["dy"].view(-1, H)[r0:r0 + rows],
+                 dh=gr["dh_out"].view(-1, H)[r0:r0 + rows])
+        s["h"] = torch.empty((rows, H), device=self.dev, dtype=tdt)
+        s["y"] = torch.empty((rows, H), device=self.dev, dtype=tdt)
+        s["mask"] = torch.empty((rows, H), device=self.dev, dtype=torch.uint8) if w.p > 0 else None
+        s["rstd"] = torch.empty(rows, device=self.dev)
+        s["mean"] = torch.empty(rows, device=self.dev) if w.norm == "ln" else None
+        s["y_hp"] = torch.empty((self.T, rows, H // self.T), device=self.dev, dtype=tdt)
+        s["y_sp"] = torch.empty((rows, H), device=self.dev, dtype=tdt)
+        s["d_res"] = torch.empty((rows, H), device=self.dev, dtype=tdt)
+        s["d_sum"] = torch.empty((rows, H), device=self.dev, dtype=tdt)
+        s["dgamma"] = torch.empty(H, device=self.dev)
+        s["dbeta"] = torch.empty(H, device=self.dev) if w.norm == "ln" else None
+        s["ws"] = self.ops.workspace_for(self.desc, self.dev)
+        return s
+
+    def set_bytes(self, s):
+        T = self.torch
+        return sum(v.numel() * v.element_size() for k, v in s.items()
+                   if isinstance(v, T.Tensor)) + sum(p.numel() * p.element_size() for p in s["partials"])
+
+    # ---- launches ---------------------------------------------------------
+    def fwd(self, s, mask_free=False):
+        self.ops.sp_rs_dropout_residual_norm_fwd(self.desc, s["partials"], s["residual"], s["gamma"],
+                                                 s["beta"], s["h"], s["y"],
+                                                 None if mask_free else s["mask"], s["rstd"], s["mean"])
+
+    def bwd(self, s, mask_free=False):
+        self.ops.sp_rs_dropout_residual_norm_bwd(self.desc, s["dy"], s["dh"], s["h"], s["gamma"],
+                                                 None if mask_free else s["mask"], s["rstd"], s["mean"],
+                                                 s["d_res"], s["d_sum"], s["dgamma"], s["dbeta"], s["ws"])
+
+    def sp2hp(self, s):
+        self.ops.sp2hp(s["y"], s["y_hp"], self.rows, self.H, self.T, self.w.dtype)
+
+    def hp2sp(self, s):
+        self.ops.hp2sp(s["y_hp"], s["y_sp"], self.rows, self.H, self.T, self.w.dtype)
+
+    def step(self, s, mask_free=False):
+        # the layout transforms of y and the backward both depend only on the
+        # forward: they run as two concurrent branches of the step
+        torch = self.torch
+        self.fwd(s, mask_free)
+        cur = torch.cuda.current_stream()
+        self.side.wait_stream(cur)
+        with torch.cuda.stream(self.side):
+            self.sp2hp(s)
+            self.hp2sp(s)
+        self.bwd(s, mask_free)
+
+    def record_steps(self, n, start, mask_free=False):
+        """n consecutive steps from set `start`; the layout branch joins the
+        main stream once per rotation over the sets and at the end (no step in
+        between touches the buffers it reads or writes)."""
+        cur = self.torch.cuda.current_stream()
+        for i in range(n):
+            k = (start + i) % self.n_sets
+            self.step(self.sets[k], mask_free)
+            if k == self.n_sets - 1 or i == n - 1:
+                cur.wait_stream(self.side)
+
+    def capture(self, fn):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.cap_stream, capture_error_mode="relaxed"):
+            fn()
+        return g
+
+    def time_launches(self, fn, reps, per_graph=None):
+        """Mean duration of one launch of fn over the rotating sets, launched
+        back to back from one CUDA graph (median over `reps` replays)."""
+        torch = self.torch
+        per_graph = per_graph or self.n_sets * max(1, -(-16 // self.n_sets))
+        g = self.capture(lambda: [fn(self.sets[i % self.n_sets]) for i in range(per_graph)])
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        evs[0].record()
+        for i in range(reps):
+            g.replay()
+            evs[i + 1].record()
+        torch.cuda.synchronize()
+        return float(np.median([evs[i].elapsed_time(evs[i + 1]) for i in range(reps)])) / per_graph
+
+    def time_single(self, fn, reps=50, warm=10):
+        """One launch at a time: events around it, a synchronize after each,
+        so launch latency is included (median)."""
+        torch = self.torch
+        out = []
+        for i in range(warm + reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn(self.sets[i % self.n_sets])
+            b.record()
+            torch.cuda.synchronize()
+            if i >= warm:
+                out.append(a.elapsed_time(b))
+        return float(np.median(out))
+
+
+def _kernel_entry(ms, nbytes, hbm_peak, single=None):
+    gbs = nbytes / (ms / 1e3) / 1e9
+    d = {"launch_ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
+         "frac_of_measured": round(gbs / hbm_peak, 4), "frac_of_nominal_8000": round(gbs / NOMINAL_HBM_GBS, 4)}
+    if single is not None:
+        d["single_launch_ms"] = round(single, 5)
+    return d
+
+
+def measure_workload(w, dev, hbm_peak, cpu_seconds=None):
+    """Per-kernel back-to-back launch times and the step time of another
+    workload (all its shards in one call), on sets rotating past the L2."""
+    import torch
+
+    hn = Harness(w, dev, 0, w.T)
+    rows = hn.rows
+    for s in hn.sets:
+        hn.step(s)
+    torch.cuda.current_stream().wait_stream(hn.side)
+    torch.cuda.synchronize()
+    reps = 20
+    per_graph = max(8, hn.n_sets)
+    t_fwd = hn.time_launches(hn.fwd, reps, per_graph)
+    t_bwd = hn.time_launches(hn.bwd, reps, per_graph)
+    t_sp2hp = hn.time_launches(hn.sp2hp, reps, per_graph)
+    g = hn.capture(lambda: hn.record_steps(per_graph, 0))
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    evs[0].record()
+    for i in range(reps):
+        g.replay()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    step_ms = float(np.median([evs[i].elapsed_time(evs[i + 1]) for i in range(reps)])) / per_graph
+    out = {"config": f"T={w.T} S={w.S} B={w.B} H={w.H} {w.dtype} {w.norm} p={w.p}, all {w.T} shards "
+                     f"in one call; {hn.n_sets} buffer sets",
+           "tokens_per_step": rows, "step_ms": round(step_ms, 5),
+           "tokens_per_s": round(rows / (step_ms / 1e3), 1),
+           "per_kernel": {"fwd": _kernel_entry(t_fwd, fwd_bytes(w, rows), hbm_peak),
+                          "bwd": _kernel_entry(t_bwd, bwd_bytes(w, rows), hbm_peak),
+                          "sp2hp": _kernel_entry(t_sp2hp, layout_bytes(w, rows), hbm_peak)}}
+    del hn, g
+    torch.cuda.empty_cache()
+    if cpu_seconds:
+        out["cpu_baseline"] = cpu_baseline(w, cpu_seconds)
+    return out
+
+
+def measure_layout(dev, hbm_peak):
+    """sp2hp and hp2sp alone on the layout workload (T=4, N=16384 tokens,
+    H=4096, bf16), back to back over sets rotating past the L2."""
+    import torch
+
+    from residual_sp_rs_gb300 import ops, synthetic as syn
+
+    lw = syn.LAYOUT
+    nbytes = 2 * lw.N * lw.H * 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(2, -(-2 * l2 // nbytes) + 1)
+    xs = [syn.layout_input(lw, dev, seed=lw.input_seed + k) for k in range(n_sets)]
+    hps = [torch.empty((lw.T, lw.N, lw.H // lw.T), device=dev, dtype=torch.bfloat16) for _ in xs]
+    backs = [torch.empty_like(x) for x in xs]
+    cap = torch.cuda.Stream()
+    res = {}
+    for name, fn in (("sp2hp", lambda k: ops.sp2hp(xs[k], hps[k], lw.N, lw.H, lw.T, lw.dtype)),
+                     ("hp2sp", lambda k: ops.hp2sp(hps[k], backs[k], lw.N, lw.H, lw.T, lw.dtype))):
+        for k in range(n_sets):
+            fn(k)
+        per_graph = max(8, n_sets)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+            for i in range(per_graph):
+                fn(i % n_sets)
+        g.replay()
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(21)]
+        evs[0].record()
+        for i in range(20):
+            g.replay()
+            evs[i + 1].record()
+        torch.cuda.synchronize()
+        ms = float(np.median([evs[i].elapsed_time(evs[i + 1]) for i in range(20)])) / per_graph
+        res[name] = _kernel_entry(ms, nbytes, hbm_peak)
+    torch.cuda.synchronize()
+    ok = torch.equal(backs[0], xs[0])
+    del xs, hps, backs
+    torch.cuda.empty_cache()
+    return {"config": f"T={lw.T} N={lw.N} H={lw.H} {lw.dtype}; {n_sets} buffer sets",
+            "roundtrip_identity": ok, "per_kernel": res}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -213,126 +505,55 @@ def run_ours(args):
     if args.seq:
         w = w.with_(S=args.seq)
     T, H = w.T, w.H
-    rows = w.S * w.B
-    tdt = syn.torch_dtype(w.dtype)
-    desc = ops.make_desc(T, 0, w.S, w.B, H, w.dtype, w.norm, w.p, w.eps, w.seed, nshards=T)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    j, nshards, dp = tp_dp_rank(rank, world, T)
+    K = args.steps
+    G = graph_steps(K)
+    # as many sets as the rotation needs, arranged so that graphs of G steps
+    # continue the rotation from replay to replay
+    hn = Harness(w, dev, j, nshards, seed_offset=dp, sets_for=lambda need: graph_rotation(G, need)[0])
+    n_sets = hn.n_sets
+    variants = n_sets // G if G < n_sets else 1
+    rows = hn.rows
 
-    def make_set(k):
-        inp = syn.fwd_inputs(w, dev, seed=w.input_seed + 17 * k)
-        gr = syn.upstream_grads(w, dev, seed=w.input_seed + 17 * k)
-        s = dict(partials=inp["partials"], residual=inp["residual"].view(rows, H),
-                 gamma=inp["gamma"], beta=inp["beta"], dy=gr["dy"].view(rows, H),
-                 dh=gr["dh_out"].view(rows, H))
-        s["h"] = torch.empty((rows, H), device=dev, dtype=tdt)
-        s["y"] = torch.empty((rows, H), device=dev, dtype=tdt)
-        s["mask"] = torch.empty((rows, H), device=dev, dtype=torch.uint8) if w.p > 0 else None
-        s["rstd"] = torch.empty(rows, device=dev)
-        s["mean"] = torch.empty(rows, device=dev) if w.norm == "ln" else None
-        s["y_hp"] = torch.empty((T, rows, H // T), device=dev, dtype=tdt)
-        s["y_sp"] = torch.empty((rows, H), device=dev, dtype=tdt)
-        s["d_res"] = torch.empty((rows, H), device=dev, dtype=tdt)
-        s["d_sum"] = torch.empty((rows, H), device=dev, dtype=tdt)
-        s["dgamma"] = torch.empty(H, device=dev)
-        s["dbeta"] = torch.empty(H, device=dev) if w.norm == "ln" else None
-        s["ws"] = ops.workspace_for(desc, dev)
-        return s
-
-    def set_bytes(s):
-        return sum(v.numel() * v.element_size() for k, v in s.items()
-                   if isinstance(v, torch.Tensor)) + sum(p.numel() * p.element_size()
-                                                         for p in s["partials"])
-
-    first = make_set(0)
-    per_set = set_bytes(first)
-    n_sets = rotation_sets(l2, per_set, fwd_bytes(w, rows), bwd_bytes(w, rows), layout_bytes(w, rows))
-    sets = [first] + [make_set(k) for k in range(1, n_sets)]
-
-    def fwd(s, stream=None, mask_free=False):
-        ops.sp_rs_dropout_residual_norm_fwd(desc, s["partials"], s["residual"], s["gamma"], s["beta"],
-                                            s["h"], s["y"], None if mask_free else s["mask"], s["rstd"],
-                                            s["mean"], stream)
-
-    def bwd(s, stream=None, mask_free=False):
-        ops.sp_rs_dropout_residual_norm_bwd(desc, s["dy"], s["dh"], s["h"], s["gamma"],
-                                            None if mask_free else s["mask"],
-                                            s["rstd"], s["mean"], s["d_res"], s["d_sum"], s["dgamma"],
-                                            s["dbeta"], s["ws"], stream=stream)
-
-    side = torch.cuda.Stream()
-
-    def step(s, join=True, mask_free=False):
-        # the layout transforms of y and the backward both depend only on the
-        # forward: they run as two concurrent branches of the step
-        fwd(s, mask_free=mask_free)
-        cur = torch.cuda.current_stream()
-        side.wait_stream(cur)
-        with torch.cuda.stream(side):
-            ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype)
-            ops.hp2sp(s["y_hp"], s["y_sp"], rows, H, T, w.dtype)
-        bwd(s, mask_free=mask_free)
-        if join:
-            cur.wait_stream(side)
-
-    # a graph replay boundary costs a few microseconds (the next replay starts
-    # only when the previous one has finished, with no programmatic dependent
-    # launch across them): one graph holds enough rotations for about 64 steps
-    n_rot = max(1, -(-64 // n_sets))
-    steps_per_graph = n_rot * n_sets
-
-    def rotations(mask_free=False):
-        # n_rot times n_sets consecutive steps, step k on buffer set k % n_sets;
-        # the layout branch of a step joins the main stream at the end of its
-        # rotation (no step in between touches its buffers)
-        for _ in range(n_rot):
-            for s in sets:
-                step(s, join=False, mask_free=mask_free)
-            torch.cuda.current_stream().wait_stream(side)
-
-    for s in sets:
-        step(s)
+    for s in hn.sets:
+        hn.step(s)
+    torch.cuda.current_stream().wait_stream(hn.side)
     torch.cuda.synchronize()
-    # one CUDA graph for a whole rotation (programmatic dependent launch then
-    # also links one step's last kernel to the next step's first), and one
-    # single-step graph per set for a remainder of steps
-    cap_stream = torch.cuda.Stream()
-    g_rot = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_rot, stream=cap_stream, capture_error_mode="relaxed"):
-        rotations()
-    graphs = []
-    for s in sets:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="relaxed"):
-            step(s)
-        graphs.append(g)
+    graphs = [hn.capture(lambda v=v: hn.record_steps(G, (v * G) % n_sets)) for v in range(variants)]
     torch.cuda.synchronize()
+    state = {"v": 0}
 
     def run_steps(k):
-        for _ in range(k // steps_per_graph):
-            g_rot.replay()
-        for i in range(k % steps_per_graph):
-            graphs[i % n_sets].replay()
+        # k a multiple of G: consecutive variants continue the rotation
+        for _ in range(k // G):
+            graphs[state["v"]].replay()
+            state["v"] = (state["v"] + 1) % variants
 
-    run_steps(args.warmup)
+    run_steps(max(args.warmup, 3) // G * G or G)
     torch.cuda.synchronize()
 
-    # ---- timed region ----------------------------------------------------------
+    # ---- timed region: runs of exactly K steps, repeated to >= 50 ms -------------
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     time.sleep(0.2)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    run_steps(args.steps)
-    ev1.record()
-    torch.cuda.synchronize()
+
+    def one_run():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run_steps(K)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    runs = timed_runs(one_run)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-    ms_per_step = ms / args.steps
-    value = weak_scaling_tokens_per_s(rows, args.steps, world, ms)
+    ms = max_over_ranks(float(np.median(runs)), world, dev)
+    ms_per_step = ms / K
+    value = weak_scaling_tokens_per_s(rows, K, world, ms)
     step_bytes = fwd_bytes(w, rows) + bwd_bytes(w, rows) + 2 * layout_bytes(w, rows)
     step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
 
@@ -341,67 +562,40 @@ def run_ours(args):
     # traffic, Philox twice
     mask_free = None
     if w.p > 0:
-        g_mf = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_mf, stream=cap_stream, capture_error_mode="relaxed"):
-            rotations(mask_free=True)
-        for _ in range(3):
-            g_mf.replay()
+        gmf = [hn.capture(lambda v=v: hn.record_steps(G, (v * G) % n_sets, mask_free=True))
+               for v in range(variants)]
+        for g in gmf:
+            g.replay()
         torch.cuda.synchronize()
-        reps_mf = max(5, min(args.steps, 20000) // steps_per_graph)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps_mf):
-            g_mf.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        ms_mf = max_over_ranks(e0.elapsed_time(e1), world, dev) / (reps_mf * steps_per_graph)
+        mf = {"v": 0}
+
+        def one_mf():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(K // G):
+                gmf[mf["v"]].replay()
+                mf["v"] = (mf["v"] + 1) % variants
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+
+        ms_mf = max_over_ranks(float(np.median(timed_runs(one_mf))), world, dev) / K
         mask_free = {"ms_per_step": round(ms_mf, 6),
                      "value": round(weak_scaling_tokens_per_s(rows, 1, world, ms_mf), 1),
-                     "unit": "tokens/s", "steps": reps_mf * steps_per_graph,
+                     "unit": "tokens/s",
                      "note": "same step with the mask pointers NULL: the forward keeps no mask, the "
                              "backward regenerates the keep bits from the seed"}
+        del gmf
 
     # ---- per-launch durations of the main kernels: each kernel alone, launched
     # back to back from one CUDA graph over the rotating sets, CUDA events
     # around the replays on the launching stream
-    def time_launches(fn, reps):
-        per_graph = steps_per_graph
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="relaxed"):
-            for i in range(per_graph):
-                fn(sets[i % n_sets])
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-        evs[0].record()
-        for i in range(reps):
-            g.replay()
-            evs[i + 1].record()
-        torch.cuda.synchronize()
-        # median over replays of the mean launch duration within a replay
-        return float(np.median([evs[i].elapsed_time(evs[i + 1]) for i in range(reps)])) / per_graph
-
-    def time_single(fn, reps=50, warm=10):
-        """One launch at a time: events around it, a synchronize after each,
-        so launch latency is included (median)."""
-        out = []
-        for i in range(warm + reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn(sets[i % n_sets])
-            b.record()
-            torch.cuda.synchronize()
-            if i >= warm:
-                out.append(a.elapsed_time(b))
-        return float(np.median(out))
-
-    reps = max(50, args.roofline_iters // steps_per_graph)
-    t_fwd = time_launches(fwd, reps)
-    t_bwd = time_launches(bwd, reps)
-    t_sp2hp = time_launches(lambda s: ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype), reps)
-    single = {"fwd": time_single(fwd), "bwd": time_single(bwd),
-              "sp2hp": time_single(lambda s: ops.sp2hp(s["y"], s["y_hp"], rows, H, T, w.dtype))}
+    per_graph = n_sets * max(1, -(-64 // n_sets))
+    reps = max(50, args.roofline_iters // per_graph)
+    t_fwd = hn.time_launches(hn.fwd, reps, per_graph)
+    t_bwd = hn.time_launches(hn.bwd, reps, per_graph)
+    t_sp2hp = hn.time_launches(hn.sp2hp, reps, per_graph)
+    single = {"fwd": hn.time_single(hn.fwd), "bwd": hn.time_single(hn.bwd), "sp2hp": hn.time_single(hn.sp2hp)}
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -409,8 +603,8 @@ def run_ours(args):
         pass
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    kern = {"fwd": (t_fwd, fwd_bytes(w, rows), "sp_fwd_kernel"),
-            "bwd": (t_bwd, bwd_bytes(w, rows), "sp_bwd_kernel+sp_colsum_kernel"),
+    kern = {"fwd": (t_fwd, fwd_bytes(w, rows), "sp_fwd_tma_kernel"),
+            "bwd": (t_bwd, bwd_bytes(w, rows), "sp_bwd_tma_kernel+sp_colsum_kernel"),
             "sp2hp": (t_sp2hp, layout_bytes(w, rows), "sp_layout_kernel")}
     dom = max(("fwd", "bwd"), key=lambda k: kern[k][0])
     d_ms, d_bytes, d_name = kern[dom]
@@ -418,12 +612,7 @@ def run_ours(args):
     traffic = None
     try:
         tr = json.load(open(os.path.join(ROOT, "profiles", f"{dom}_{args.workload}_traffic.json")))
-        from residual_sp_rs_gb300.build import _deps
-        import hashlib
-        h = hashlib.sha256()
-        for p in sorted(_deps()):
-            h.update(open(p, "rb").read())
-        if tr.get("source_sha256") == h.hexdigest():
+        if tr.get("source_sha256") == spbuild.source_hash() and world == 1 and not args.seq:
             traffic = tr.get("bytes_per_launch")
     except (OSError, ValueError):
         pass
@@ -436,52 +625,75 @@ def run_ours(args):
                                  "launches over the rotating buffer sets; single_launch_ms: median "
                                  "of 50 launches each alone between events and a synchronize "
                                  "(includes launch latency)",
-                "per_kernel": {k: {"launch_ms": round(v[0], 5), "single_launch_ms": round(single[k], 5),
-                                   "algorithmic_bytes": v[1],
-                                   "gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1),
-                                   "frac_of_measured": round(v[1] / (v[0] / 1e3) / 1e9 / hbm_peak, 4),
-                                   "frac_of_nominal_8000": round(v[1] / (v[0] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-                                                                 4)}
-                               for k, v in kern.items()}}
+                "per_kernel": {k: _kernel_entry(v[0], v[1], hbm_peak, single[k]) for k, v in kern.items()}}
 
     # ---- end to end: pinned host inputs in, results out, every step -------------
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, desc, dev, sets, rows, world)
+        e2e = run_e2e(args, w, hn, world)
+    del graphs, hn
+    torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, args.cpu_seconds)
 
+    # ---- the other workloads (one GPU only: per-kernel figures) -----------------
+    extra = None
+    if world == 1 and not args.no_extra and not args.seq:
+        extra = {}
+        cpu_s = None if args.no_cpu else 4.0
+        for key, name, p in EXTRA_WORKLOADS:
+            wx = syn.WORKLOADS[name] if p is None else syn.WORKLOADS[name].with_(p=p)
+            extra[key] = measure_workload(wx, dev, hbm_peak, cpu_s)
+        extra["layout_bf16"] = measure_layout(dev, hbm_peak)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
             if w.dtype == "bf16" else "f32", "data": "synthetic (seeded torch.Generator)",
             "config": {"workload": f"{w.name}: SP region fwd+sp2hp+hp2sp+bwd, T={T} S={w.S} B={w.B} "
                                    f"H={H} {w.dtype} {w.norm} p={w.p}",
                        "T": T, "S": w.S, "B": w.B, "H": H, "norm": w.norm, "p": w.p,
-                       "tokens_per_step": rows, "parallelism": f"replica x{world}",
-                       "l2": f"inputs rotate over {n_sets} buffer sets, {n_sets * per_set / 1e6:.0f} MB; "
-                             f"each kernel's own bytes over a rotation > 2x L2 ({l2 / 1e6:.0f} MB)",
-                       "launch": f"one CUDA graph replay per {steps_per_graph} steps ({n_rot} rotations "
-                                 f"over the {n_sets} buffer sets; layout branch concurrent with the "
-                                 "backward, joined once per rotation), programmatic dependent launch "
-                                 "between the kernels of a replay; single-step graphs for a remainder"},
-            "hbm_gbs_step": round(step_gbs, 1),
-            "hbm_frac_step": round(step_gbs / hbm_peak, 4),
-            "hbm_frac_step_of_nominal_8000": round(step_gbs / NOMINAL_HBM_GBS, 4),
+                       "tokens_per_step_per_gpu": rows,
+                       "parallelism": ("one GPU plays the whole tensor-parallel group (all shards)"
+                                       if world == 1 else
+                                       f"rank r runs sequence shard r % {T} of data-parallel replica "
+                                       f"r // {T} ({world} ranks)"),
+                       "l2": f"inputs rotate over {n_sets} buffer sets, {n_sets * hn_set_mb(w, rows):.0f} MB; "
+                             "between two uses of a set each kernel's own bytes exceed 2x L2",
+                       "launch": f"timed run = exactly {K} steps from CUDA graphs of {G} steps "
+                                 f"({variants} graph variant(s) continuing the rotation), programmatic "
+                                 "dependent launch between the kernels of a graph; the layout branch is "
+                                 "concurrent with the backward; median of "
+                                 f"{len(runs)} timed runs ({sum(runs):.1f} ms in all)"},
+            "step_algorithmic_gbs": round(step_gbs, 1),
+            "step_algorithmic_gbs_note": "algorithmic bytes of the step's five launches / step time; "
+                                         "the backward's reads of h and mask and the layout's read of y "
+                                         "are served from L2 right after the forward wrote them, so this "
+                                         "is not a DRAM rate",
             "roofline": roofline,
-            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "gpu_launches": LAUNCHES_PER_STEP * K * len(runs),
+            "gpu_launches_note": f"{LAUNCHES_PER_STEP} launches per step x {K} steps x {len(runs)} timed runs",
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "mask_free": mask_free,
+            "workloads": extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, desc, dev, sets, rows, world):
+def hn_set_mb(w, rows):
+    """Approximate bytes of one buffer set (MB), for the config note."""
+    e = 2 if w.dtype == "bf16" else 4
+    full = w.S * w.B * w.H * e
+    per_rows = rows * w.H * e
+    return (w.T * full + 2 * full + per_rows * 8 + rows * w.H) / 1e6
+
+
+def run_e2e(args, w, hn, world):
     """Through the public API with HOST buffers: every step copies its inputs
     from pinned host memory, runs the step and copies its results back.  The
     steps run as a three-stage pipeline on two device buffer sets (inputs in
@@ -492,12 +704,14 @@ def run_e2e(args, w, desc, dev, sets, rows, world):
 
     from residual_sp_rs_gb300 import ops
 
-    T, H = w.T, w.H
+    T, H, rows, row0 = w.T, w.H, hn.rows, hn.row0
+    desc, dev, sets = hn.desc, hn.dev, hn.sets
     s0 = sets[0]
+    rowb = H * (2 if w.dtype == "bf16" else 4)
 
     # a step's inputs travel as one block and its results as another: one
-    # copy each way per step
-    in_named = [(f"P{t}", p.view(rows, H)) for t, p in enumerate(s0["partials"])]
+    # copy each way per step; only this rank's rows of each partial travel
+    in_named = [(f"P{t}", p.view(-1, H)[row0:row0 + rows]) for t, p in enumerate(s0["partials"])]
     in_named += [(k, s0[k]) for k in ("residual", "dy", "dh", "gamma", "beta") if s0[k] is not None]
     out_named = [(k, s0[k]) for k in ("y", "d_res", "d_sum", "dgamma", "dbeta") if s0[k] is not None]
     host_in, hv = packed_block(in_named, "cpu", pin=True)
@@ -509,7 +723,9 @@ def run_e2e(args, w, desc, dev, sets, rows, world):
         fi, vi = packed_block(in_named, dev)
         fo, vo = packed_block(out_named, dev)
         d = dict(sets[k])
-        d["partials"] = vi[:T]
+        # the call addresses partial t by global row (shard j's rows start at
+        # row j*R), so it gets the address row0 rows before the resident rows
+        d["partials"] = [v.data_ptr() - row0 * rowb for v in vi[:T]]
         d.update({name: v for (name, _), v in zip(in_named[T:], vi[T:])})
         d.update({name: v for (name, _), v in zip(out_named, vo)})
         dsets.append(d)
@@ -554,7 +770,7 @@ def run_e2e(args, w, desc, dev, sets, rows, world):
         one_step(i)
     b.record(st_out)  # after the last step's results are on the host
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
     return {"value": round(rows * args.e2e_steps * world / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps,
             "ms_per_step": round(ms / args.e2e_steps, 5),
@@ -633,6 +849,9 @@ def cpu_baseline(w, seconds):
 
 
 def _cpu_baseline(w, seconds, core):
+    # the oracle's cost per token row does not depend on S: draw the inputs
+    # for a short sequence of the same shape and cycle over its rows
+    w = w.with_(S=min(w.S, w.T * max(1, 128 // w.B)))
     oracle, st = _oracle_setup(w)
     rows = w.S * w.B
     n = max(w.T, (64 // w.T) * w.T)
@@ -644,9 +863,9 @@ def _cpu_baseline(w, seconds, core):
         row0 = (row0 + n) % (rows - n + 1)
     dt = time.perf_counter() - t0
     return {"value": round(done / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} token rows ({done / rows:.2f} of one step's {rows}) of the same "
-                      f"workload through the fp64 oracle (fwd, sp2hp, hp2sp, bwd), {dt:.1f} s, "
-                      + _host_note(core)}
+            "sample": f"{done} token rows of the workload's shape (T={w.T}, H={w.H}, {w.dtype}, "
+                      f"{w.norm}, p={w.p}; inputs drawn for S={w.S}, rows cycled) through the fp64 "
+                      f"oracle (fwd, sp2hp, hp2sp, bwd), {dt:.1f} s, " + _host_note(core)}
 
 
 def run_reference(args):

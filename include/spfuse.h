@@ -77,7 +77,21 @@ typedef struct sp_rs_desc_t {
   uint64_t seed;    /* Philox4x32-10 key of the dropout mask */
   int32_t nshards;  /* shards j .. j+nshards-1 in one call; 0 is read as 1 */
   int32_t reserved; /* must be 0 */
+  uint32_t* status; /* optional DEVICE word, or NULL; see "Device status" below */
 } sp_rs_desc_t;
+
+/* Device status.  Every wait of a kernel on data in flight (a bulk copy
+ * landing in shared memory, a ring stage being released) is bounded: after
+ * about two seconds the waiting threads give up, mark the results they could
+ * not compute (NaN in rstd for the forward's unfinished rows, NaN in every
+ * dgamma/dbeta element for the backward), let the copies they started land
+ * and return, so the GPU and the CUDA context stay usable.  When desc->status
+ * is not NULL, such a kernel also ORs one of the bits below into that 4-byte
+ * aligned device word (atomically).  The library never clears the word: the
+ * caller zeroes it, runs any number of calls and reads it back whenever it
+ * likes (e.g. once per training step).  A clean run leaves it unchanged. */
+#define SP_DEVICE_FWD_WAIT_TIMEOUT 0x1u /* a forward kernel gave up waiting */
+#define SP_DEVICE_BWD_WAIT_TIMEOUT 0x2u /* a backward kernel gave up waiting */
 
 /* Forward of the SP region for sequence shards j .. j+nshards-1.
  *
@@ -95,7 +109,11 @@ typedef struct sp_rs_desc_t {
  *             computed from the stored h.
  *
  * partials : host array of T device pointers, each a full [S,B,H] tensor
- *            (16-byte aligned).  Only rows of the processed shards are read.
+ *            (16-byte aligned).  Only rows [j*R, (j+nshards)*R) of each are
+ *            read, by their global row index: a caller that holds only those
+ *            rows of partial t (a rank that received its shard's block of
+ *            every partial, [MT3] §3.2.3) passes the address its row 0 would
+ *            have, i.e. the block's address minus j*R*H*element bytes.
  * residual : [nshards*R, H] residual stream of those shards.
  * gamma    : [H]; beta: [H] for LayerNorm (ignored for RMSNorm).
  * h_out, y_out : [nshards*R, H] outputs (residual stream, norm output).
@@ -219,6 +237,10 @@ const char* sp_last_cuda_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t sp_version(void);
 
+/* SHA-256 (hex) of the sources the library was built from, so a binding can
+ * refuse a library that does not match its tree. */
+const char* sp_build_hash(void);
+
 /* The launch configuration of one TMA-fed kernel (all fields 0 when the
  * register-resident kernel would run instead).  Sizes in bytes. */
 typedef struct sp_kernel_plan_t {
@@ -231,11 +253,14 @@ typedef struct sp_kernel_plan_t {
   int32_t rows_per_stage; /* rows per shared-memory ring stage (1 when chunked) */
   int32_t stages;         /* ring stages */
   int32_t chunked;        /* forward only: a stage holds one column chunk of a row */
-  int32_t reserved;
+  int32_t noalloc_fits;   /* backward only: 1 when workspace_bytes fits the fixed scratch of
+                             sp_rs_dropout_residual_norm_bwd_noalloc (which refuses the call
+                             otherwise), 0 when it does not */
   int64_t stage_bytes;    /* one ring stage, all inputs */
   int64_t smem_bytes;     /* dynamic shared memory per CTA */
   int64_t rows_per_cta;   /* contiguous token rows each CTA owns */
   int64_t ctas;           /* grid size */
+  int64_t workspace_bytes; /* backward only: sp_rs_bwd_workspace_bytes on such a device */
 } sp_kernel_plan_t;
 
 typedef struct sp_plan_info_t {

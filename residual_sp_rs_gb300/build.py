@@ -1,12 +1,15 @@
 """Build libspfuse.so in-tree with nvcc for sm_103a.
 
 Each translation unit is compiled in parallel, then linked into one shared
-library (static CUDA runtime, no torch dependency).  Rebuilds only when a
-source is newer than the library.
+library (static CUDA runtime, no torch dependency).  The library carries the
+SHA-256 of the sources it was built from (exported as sp_build_hash(), and
+written beside it as libspfuse.so.sha256); it is rebuilt whenever that hash
+is not the hash of the current sources.
 """
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -18,6 +21,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspfuse.so")
+HASH_PATH = LIB_PATH + ".sha256"
 BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,11 +45,23 @@ def _deps() -> list[str]:
         + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
+def source_hash() -> str:
+    """SHA-256 over the library's sources (names relative to the package and
+    contents, in a fixed order) and the compiler flags."""
+    h = hashlib.sha256()
+    for p in sorted(_deps(), key=lambda q: os.path.relpath(q, ROOT)):
+        h.update(os.path.relpath(p, ROOT).encode() + b"\0")
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS[:8]).encode())
+    return h.hexdigest()
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+    if not (os.path.exists(LIB_PATH) and os.path.exists(HASH_PATH)):
         return False
-    lib_t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(d) <= lib_t for d in _deps())
+    with open(HASH_PATH) as f:
+        return f.read().strip() == source_hash()
 
 
 def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
@@ -53,7 +69,9 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
+    digest = source_hash()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    extra += [f"-DSPF_SOURCE_HASH=\"{digest}\""]
 
     def compile_one(src: str) -> tuple[str, str]:
         obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
@@ -75,6 +93,9 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    with open(HASH_PATH + f".tmp{os.getpid()}", "w") as f:
+        f.write(digest + "\n")
+    os.replace(HASH_PATH + f".tmp{os.getpid()}", HASH_PATH)
     return LIB_PATH
 
 

@@ -29,6 +29,26 @@ bool inject_launch_failure() {
   return on;
 }
 
+// Test hooks for the bounded waits, read once per process: SPFUSE_TEST_WAIT_NS
+// shortens the limit of every mbarrier wait (nanoseconds) and
+// SPFUSE_TEST_DROP_STAGE makes the producer of CTA 0 of the TMA-fed kernels
+// skip that ring stage, so the waits on it run out and the kernels take
+// their timeout path (no fault, no hang: every wait returns).
+struct WaitHooks {
+  uint64_t wait_ns;
+  int32_t drop_stage;
+};
+
+const WaitHooks& wait_hooks() {
+  static const WaitHooks h = [] {
+    WaitHooks w{kWaitNs, -1};
+    if (const char* e = std::getenv("SPFUSE_TEST_WAIT_NS")) w.wait_ns = std::strtoull(e, nullptr, 10);
+    if (const char* e = std::getenv("SPFUSE_TEST_DROP_STAGE")) w.drop_stage = std::atoi(e);
+    return w;
+  }();
+  return h;
+}
+
 // The CUDA error behind the last SP_ERR_CUDA on this host thread.
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
@@ -55,6 +75,7 @@ sp_status_t check_desc(const sp_rs_desc_t* d, Problem* pr) {
     return SP_ERR_INVALID_ARG;
   if (!(d->p >= 0.0f && d->p < 1.0f)) return SP_ERR_INVALID_ARG;
   if (!(d->eps > 0.0f) || !std::isfinite(d->eps)) return SP_ERR_INVALID_ARG;
+  if (!aligned(d->status, 4)) return SP_ERR_ALIGN;
   if (d->S < 0 || d->B < 0 || d->H <= 0) return SP_ERR_SHAPE;
   if (d->S % d->T != 0) return SP_ERR_SHAPE;
   const int ev = 16 / elem_bytes(d->dtype);
@@ -217,6 +238,9 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   a.Hf = (float)pr.H;
   a.dropout = desc->p > 0.0f ? 1 : 0;
   a.dyadic_scale = a.scale_lo == 0.0f ? 1 : 0;
+  a.status = desc->status;
+  a.wait_ns = wait_hooks().wait_ns;
+  a.drop_stage = wait_hooks().drop_stage;
 
   if (inject_launch_failure()) return SP_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -314,6 +338,9 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc, const void
     a.nparts = pl.nparts;
     a.scale = (float)(1.0 / (1.0 - (double)desc->p));
     a.Hf = (float)pr.H;
+    a.status = desc->status;
+    a.wait_ns = wait_hooks().wait_ns;
+    a.drop_stage = wait_hooks().drop_stage;
     cudaError_t e;
     if (pl.tma) {
       a.tpr = pl.tp.shape.tpr;
@@ -366,7 +393,12 @@ const char* sp_status_string(sp_status_t s) {
   }
 }
 
-int32_t sp_version(void) { return 200; }
+int32_t sp_version(void) { return 300; }
+
+#ifndef SPF_SOURCE_HASH
+#define SPF_SOURCE_HASH "unknown"
+#endif
+const char* sp_build_hash(void) { return SPF_SOURCE_HASH; }
 
 sp_status_t sp_plan_describe(const sp_rs_desc_t* desc, int32_t sms, int32_t smem_optin,
                              int32_t has_dh, int32_t has_mask, sp_plan_info_t* out) {
@@ -378,7 +410,8 @@ sp_status_t sp_plan_describe(const sp_rs_desc_t* desc, int32_t sms, int32_t smem
   if (pr.dtype != SP_BF16) return SP_OK;  // f32 runs the register-resident kernels
   const bool ln = pr.norm == SP_LAYERNORM;
   FwdTmaPlan tp;
-  if (plan_fwd_tma(pr.H, pr.T, ln, smem_optin, pr.rows, sms, &tp)) {
+  // the forward launches nothing without rows
+  if (pr.rows > 0 && plan_fwd_tma(pr.H, pr.T, ln, smem_optin, pr.rows, sms, &tp)) {
     sp_kernel_plan_t& f = out->fwd;
     f.tma = 1;
     f.block = tp.shape.block;
@@ -395,7 +428,8 @@ sp_status_t sp_plan_describe(const sp_rs_desc_t* desc, int32_t sms, int32_t smem
     f.ctas = (pr.rows + tp.layout.rows_per_cta - 1) / tp.layout.rows_per_cta;
   }
   BwdPlan bp;
-  if (plan_bwd_tma_for(pr, has_dh != 0, has_mask != 0, sms, smem_optin, &bp)) {
+  // as the backward itself: the mask is read only when p > 0
+  if (plan_bwd_tma_for(pr, has_dh != 0, has_mask != 0 && desc->p > 0.0f, sms, smem_optin, &bp)) {
     sp_kernel_plan_t& b = out->bwd;
     b.tma = 1;
     b.block = bp.tp.shape.block;
@@ -409,6 +443,8 @@ sp_status_t sp_plan_describe(const sp_rs_desc_t* desc, int32_t sms, int32_t smem
     b.smem_bytes = (int64_t)bp.tp.smem;
     b.rows_per_cta = bp.rows_per_cta;
     b.ctas = bp.ctas;
+    b.workspace_bytes = (int64_t)bp.ws_bytes;
+    b.noalloc_fits = noalloc_scratch_fits(bp.ws_bytes) ? 1 : 0;
   }
   return SP_OK;
 }

@@ -44,6 +44,8 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
   const int ns = ln ? 2 : 1;
   const uint32_t rowb = (uint32_t)H * 2;
   const size_t fixed_base = (size_t)H * 4;  // gamma, fp32
+  if (max_smem <= (int)kStaticSmem) return false;  // no room for a ring at all
+  if (max_smem <= (int)kStaticSmem) return false;  // no room for a ring at all
   const size_t budget = (size_t)max_smem - kStaticSmem;
   for (; nrg >= 1; --nrg) {
     const bool narrow = nrg * tpr + 32 <= kBwdTmaNarrow;
@@ -74,6 +76,7 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
       // at the end the ring holds the row groups' column sums
       if ((size_t)nst * L.stage_bytes < (size_t)nrg * ns * 8 * (nvec + 4) * 4) continue;
       L.nst = nst;
+      L.pf_stages = prefetch_stages(L.stage_bytes);
       L.smem_stages = (uint32_t)(16 * (((size_t)2 * nst * 8 + 15) / 16) + fixed_base);
       p->layout = L;
       p->shape.tpr = tpr;

@@ -19,8 +19,8 @@
 // CTA order.
 //
 // If a wait times out (a copy that never lands), the CTA stops, waits (with a
-// limit) for what it issued, and poisons its dgamma/dbeta partial with NaN so
-// the failure is visible in the result.
+// limit) for what it issued, poisons its dgamma/dbeta partial with NaN so the
+// failure is visible in the result, and reports it in the device status word.
 #pragma once
 
 #include "common.cuh"
@@ -30,6 +30,7 @@ namespace spf {
 
 constexpr int kBwdTmaNarrowBlock = 512;  // the 16-warp block (128 registers)
 constexpr int kBwdTmaMidBlock = 544;     // two 8-warp row groups + producer (96 registers)
+
 
 // NTHR = 512: at most 16 warps (15 consumer + 1 producer), so 128 registers
 // per thread fit every SM sub-partition's register file; the 544-thread
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
 
   // Producer: fill stage j (rows j*rb ..) of the ring.
   auto issue_stage = [&](int j, uint64_t pol) {
+    if (j == a.drop_stage && blockIdx.x == 0) return;  // test hook: this stage never lands
     const int s = j % nst;
     unsigned char* st = stages + (size_t)s * L.stage_bytes;
     const int64_t r = r0 + (int64_t)j * rb;
@@ -94,14 +96,21 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
   const bool lead = producer && lr == 0;
   int issued = 0;
   if (lead && n > 0 && n <= nst * rb) {
-    // the CTA's rows all fit the first ring: they head for L2 while the
-    // previous kernel drains (with more rows per CTA the start-up is a small
-    // share of the kernel and the early requests only compete with it)
-    const uint32_t pb = (uint32_t)(n * rowb);
-    l2_prefetch(reinterpret_cast<const char*>(a.dy) + r0 * rowb, pb);
-    l2_prefetch(reinterpret_cast<const char*>(a.h) + r0 * rowb, pb);
-    if constexpr (DH) l2_prefetch(reinterpret_cast<const char*>(a.dh) + r0 * rowb, pb);
-    if constexpr (MASK) l2_prefetch(a.mask + r0 * (int64_t)H, (uint32_t)(n * H));
+    // the CTA's rows all fit the first ring: the first pf_stages stages head
+    // for L2 while the previous kernel drains, so the first rows land early
+    // (with more rows per CTA the start-up is a small share of the kernel
+    // and early requests only compete with it).  Prefetching every stage
+    // instead measured slower: the requests of all stages then arrive
+    // together and the first rows wait for the last.
+    for (int j = 0; j < min(nstage, L.pf_stages); ++j) {
+      const int64_t r = r0 + (int64_t)j * rb;
+      const int rows = min(rb, n - j * rb);
+      const uint32_t pb = (uint32_t)(rows * rowb);
+      l2_prefetch(reinterpret_cast<const char*>(a.dy) + r * rowb, pb);
+      l2_prefetch(reinterpret_cast<const char*>(a.h) + r * rowb, pb);
+      if constexpr (DH) l2_prefetch(reinterpret_cast<const char*>(a.dh) + r * rowb, pb);
+      if constexpr (MASK) l2_prefetch(a.mask + r * (int64_t)H, (uint32_t)(rows * H));
+    }
   }
   grid_dep_wait();
   grid_dep_launch_dependents();
@@ -144,16 +153,18 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
       const uint64_t pol = policy_evict_first();
       for (int j = issued; j < nstage; ++j) {
         const int k = j / nst;  // >= 1: the slot was used k times before
-        if (!mbar_wait(&empty[j % nst], (uint32_t)((k - 1) & 1))) {
+        if (!mbar_wait(&empty[j % nst], (uint32_t)((k - 1) & 1), a.wait_ns)) {
           ok = false;
           break;
         }
         issue_stage(j, pol);
         issued = j + 1;
       }
-      // nothing may still be landing in shared memory when the CTA exits
+      // nothing may still be landing in shared memory when the ring is
+      // reused below or the CTA exits; a copy that did not land in time
+      // leaves the ring unusable
       for (int j = max(0, issued - nst); j < issued; ++j)
-        mbar_wait(&full[j % nst], (uint32_t)((j / nst) & 1));
+        if (!mbar_wait(&full[j % nst], (uint32_t)((j / nst) & 1), a.wait_ns)) ok = false;
     }
   } else {
     float* rred = red + rg * 2 * (tpr >> 5) * NS;
@@ -204,7 +215,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
       // the whole row group agrees on the outcome of the wait before any of
       // it enters the row reduction's named barrier
       // (one-warp row groups vote; wider ones use their named barrier, id <= 8)
-      const bool landed = mbar_wait(&full[s], (uint32_t)par);
+      const bool landed = mbar_wait(&full[s], (uint32_t)par, a.wait_ns);
       const bool all_landed =
           tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
       if (!all_landed) {
@@ -355,7 +366,16 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
   }
 
   if (!ok) s_failed = 1;
-  __syncthreads();  // every stage consumed and landed: the ring is free
+  __syncthreads();  // every stage consumed and landed (unless a wait timed out)
+  // A CTA whose wait timed out poisons its partial rows so dgamma/dbeta are
+  // NaN, and leaves the ring alone: a copy may still be landing there.
+  if (s_failed != 0) {
+    if (threadIdx.x == 0) report_status(a.status, kStatusBwdWaitTimeout);
+    for (int st = 0; st < NS; ++st)
+      for (int c = threadIdx.x; c < H; c += blockDim.x)
+        __stcg(a.ws + ((int64_t)st * a.nparts + blockIdx.x) * H + c, __int_as_float(0x7FC00000));
+    return;
+  }
 
   // ---- dgamma/dbeta: row groups' column sums into the ring, added in order ---
   // The ring holds them as [nrg][NS][EV][pitch], pitch = nvec + 4: element e
@@ -387,8 +407,6 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
     }
   }
   __syncthreads();
-  // a CTA whose wait timed out poisons its partial so dgamma/dbeta are NaN
-  const bool failed = s_failed != 0;
   for (int st = 0; st < NS; ++st) {
     float* dst = a.ws + ((int64_t)st * a.nparts + blockIdx.x) * H;
     for (int c = threadIdx.x; c < H; c += blockDim.x) {
@@ -404,7 +422,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
         for (int u = 0; u < 4; ++u)
           if (g0 + u < nrg) acc += t[u];
       }
-      __stcg(dst + c, failed ? __int_as_float(0x7FC00000) : acc);
+      __stcg(dst + c, acc);
     }
   }
 }

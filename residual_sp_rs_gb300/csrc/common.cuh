@@ -16,7 +16,8 @@ constexpr int kMaxT = 8;  // largest TP/SP group the kernels unroll for
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel waits for the grids it depends
 // on before its first global read, and lets the next kernel in the stream be
-// scheduled as soon as all of its own CTAs are resident.
+// scheduled as soon as all of its own CTAs are resident.  (Letting it be
+// scheduled before the wait measured the same at the pages' shape.)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -398,6 +399,9 @@ struct FwdArgs {
   float Hf;              // H as float
   int32_t dropout;       // p > 0
   int32_t dyadic_scale;  // 1/(1-p) is exact in fp32 (scale_lo == 0): bf16 ties can occur
+  uint32_t* status;      // device status word (timeouts are ORed in) or null
+  uint64_t wait_ns;      // bound of every mbarrier wait
+  int32_t drop_stage;    // test hook: CTA 0's producer never fills this stage (-1: none)
 };
 
 struct BwdArgs {
@@ -424,7 +428,18 @@ struct BwdArgs {
   uint32_t thr;          // keep threshold (regen)
   int64_t grow0;         // global row index of local row 0 (regen)
   PhiloxKeys keys;       // Philox round keys of the seed (regen)
+  uint32_t* status;      // device status word (timeouts are ORed in) or null
+  uint64_t wait_ns;      // bound of every mbarrier wait
+  int32_t drop_stage;    // test hook: CTA 0's producer never fills this stage (-1: none)
 };
+
+// Bits of the device status word (the values of include/spfuse.h).
+constexpr uint32_t kStatusFwdWaitTimeout = 0x1u;
+constexpr uint32_t kStatusBwdWaitTimeout = 0x2u;
+
+__device__ __forceinline__ void report_status(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
 
 // Shared-memory ring of the TMA-fed forward.
 struct FwdTmaLayout {
@@ -434,6 +449,7 @@ struct FwdTmaLayout {
   uint32_t stage_bytes;  // bytes of one stage
   uint32_t blk;          // bytes of one tensor's rows in a stage (rb * H * 2)
   uint32_t smem_stages;  // offset of stage 0 in dynamic shared memory
+  int32_t pf_stages;     // stages prefetched into L2 before the grid-dependency wait
   int64_t rows_per_cta;
 };
 
@@ -445,6 +461,7 @@ struct BwdTmaLayout {
   uint32_t stage_bytes; // bytes of one stage
   uint32_t off_h, off_dh, off_mask;  // offsets inside a stage (dy at 0)
   uint32_t smem_stages; // offset of stage 0 in dynamic shared memory
+  int32_t pf_stages;    // stages prefetched into L2 before the grid-dependency wait
 };
 
 }  // namespace spf

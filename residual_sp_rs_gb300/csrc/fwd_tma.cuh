@@ -24,8 +24,8 @@
 // input) -- so a row is VPT stages, each released as soon as its slot's h is
 // in registers.
 //
-// If a wait times out, the row group stops and writes NaN into the rstd of
-// the rows it did not finish, so the failure is visible in the outputs.
+// If a wait times out, the row group stops, writes NaN into the rstd of the
+// rows it did not finish and reports the timeout in the device status word.
 #pragma once
 
 #include "common.cuh"
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
   const uint64_t pol = policy_evict_first();
 
   auto issue_stage = [&](int j) {
+    if (j == a.drop_stage && blockIdx.x == 0) return;  // test hook: this stage never lands
     const int s = j % L.nst;
     unsigned char* st = stages + (size_t)s * L.stage_bytes;
     const int jr = j / NCH, k = j - jr * NCH;   // row stage and (CH) column chunk
@@ -194,13 +195,19 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
   int issued = 0;
   uint32_t keep[VPT];  // keep bits of this thread's next row, drawn ahead
   if (!CH && lead && n > 0 && n <= L.nst * L.rb) {
-    // the CTA's rows all fit the first ring: they head for L2 while the
-    // previous kernel drains (with more rows per CTA the start-up is a small
-    // share of the kernel and the early requests only compete with it)
-    const uint32_t pb = (uint32_t)(n * rowb);
+    // the CTA's rows all fit the first ring: the first pf_stages stages head
+    // for L2 while the previous kernel drains, so the first rows land early
+    // (with more rows per CTA the start-up is a small share of the kernel
+    // and early requests only compete with it).  Prefetching every stage
+    // instead measured slower: the requests of all stages then arrive
+    // together and the first rows wait for the last.
+    for (int jr = 0; jr < min(nrow_st, L.pf_stages); ++jr) {
+      const int64_t r = r0 + (int64_t)jr * L.rb;
+      const uint32_t pb = (uint32_t)(min(L.rb, n - jr * L.rb) * rowb);
 #pragma unroll
-    for (int t = 0; t < T; ++t) l2_prefetch(reinterpret_cast<const char*>(a.P[t]) + (a.grow0 + r0) * rowb, pb);
-    l2_prefetch(reinterpret_cast<const char*>(a.residual) + r0 * rowb, pb);
+      for (int t = 0; t < T; ++t) l2_prefetch(reinterpret_cast<const char*>(a.P[t]) + (a.grow0 + r) * rowb, pb);
+      l2_prefetch(reinterpret_cast<const char*>(a.residual) + r * rowb, pb);
+    }
   }
   grid_dep_wait();
   grid_dep_launch_dependents();
@@ -246,12 +253,16 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
     if (lead) {
       for (int j = issued; j < nstage; ++j) {
         const int k = j / L.nst;
-        if (!mbar_wait(&empty[j % L.nst], (uint32_t)((k - 1) & 1))) break;
+        if (!mbar_wait(&empty[j % L.nst], (uint32_t)((k - 1) & 1), a.wait_ns)) {
+          report_status(a.status, kStatusFwdWaitTimeout);
+          break;
+        }
         issue_stage(j);
         issued = j + 1;
       }
+      // nothing may still be landing in shared memory when the CTA exits
       for (int j = max(0, issued - L.nst); j < issued; ++j)
-        mbar_wait(&full[j % L.nst], (uint32_t)((j / L.nst) & 1));
+        mbar_wait(&full[j % L.nst], (uint32_t)((j / L.nst) & 1), a.wait_ns);
     }
     return;
   }
@@ -264,12 +275,12 @@ __global__ void __launch_bounds__(NTHR, 1) sp_fwd_tma_kernel(const FwdArgs a, co
   int ri = rg % L.rb, s = ((rg / L.rb) * NCH) % L.nst, par = (((rg / L.rb) * NCH) / L.nst) & 1;
   // wait for ring slot (s, par) -- the whole row group agrees -- or give up
   auto wait_stage = [&](int ws, int wpar, int i) -> bool {
-    const bool landed = mbar_wait(&full[ws], (uint32_t)wpar);
+    const bool landed = mbar_wait(&full[ws], (uint32_t)wpar, a.wait_ns);
     const bool all_landed =
         tpr == 32 ? __all_sync(0xFFFFFFFFu, landed) : bar_red_and(1 + rg, tpr, landed);
-    if (!all_landed) {  // mark this row group's unfinished rows
-      for (int k = i; k < n; k += L.nrg)
-        if (lr == 0) a.rstd[r0 + k] = __int_as_float(0x7FC00000);
+    if (!all_landed && lr == 0) {  // mark this row group's unfinished rows
+      for (int k = i; k < n; k += L.nrg) a.rstd[r0 + k] = __int_as_float(0x7FC00000);
+      report_status(a.status, kStatusFwdWaitTimeout);
     }
     return all_landed;
   };

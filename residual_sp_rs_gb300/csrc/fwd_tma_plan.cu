@@ -31,6 +31,7 @@ bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms
   const int nvec = (int)(H / 8);
   const size_t rowb = (size_t)H * 2;
   const size_t gb = (size_t)H * 4 * (ln ? 2 : 1);
+  if (max_smem <= (int)kStaticSmem) return false;  // no room for a ring at all
   const size_t budget = (size_t)max_smem - kStaticSmem;
   const int64_t ctas = rows < sms ? (rows > 0 ? rows : 1) : sms;
   const int64_t rows_per_cta = rows > 0 ? (rows + ctas - 1) / ctas : 1;
@@ -70,6 +71,7 @@ bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms
     L.blk = (uint32_t)blk;
     L.smem_stages = (uint32_t)(16 * (((size_t)2 * nst * 8 + 15) / 16) + gb);
     L.rows_per_cta = rows_per_cta;
+    L.pf_stages = prefetch_stages(stage);
     p->layout = L;
     p->shape.tpr = tpr;
     p->shape.vpt = vpt;

@@ -5,9 +5,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/spfuse.h"
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace spf {
+
+// The allocation-free backward keeps its partial rows in a fixed array of
+// SP_NOALLOC_SCRATCH_BYTES and refuses problems whose workspace exceeds it.
+inline bool noalloc_scratch_fits(size_t workspace_bytes) {
+  return workspace_bytes <= (size_t)SP_NOALLOC_SCRATCH_BYTES;
+}
+
+// The TMA-fed kernels prefetch their first ring stages into L2 before the
+// grid-dependency wait: as many stages as it takes to reach this many bytes
+// per CTA (at least one), about what keeps one SM's share of HBM busy.
+constexpr size_t kPrefetchBytes = 48 * 1024;
+inline int prefetch_stages(size_t stage_bytes) {
+  return (int)((kPrefetchBytes + stage_bytes - 1) / stage_bytes);
+}
 
 // Launch with programmatic dependent launch allowed: the kernel may be
 // scheduled while the previous kernel in the stream drains; it does not read

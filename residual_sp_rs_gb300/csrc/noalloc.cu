@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "../../include/spfuse.h"
+#include "launch.h"
 
 namespace {
 
@@ -42,12 +43,14 @@ extern "C" sp_status_t sp_rs_dropout_residual_norm_bwd_noalloc(
     const sp_rs_desc_t* desc, const void* dy, const void* dh_out, const void* h_saved,
     const void* gamma, const uint8_t* mask, const float* rstd, const float* mean,
     void* d_residual, void* d_sum, float* dgamma, float* dbeta, sp_stream_t stream) {
+  // A problem whose partial rows need more than the fixed array is refused
+  // before anything is launched (an invalid descriptor reports 0 here and is
+  // refused with its own status by the call below).
+  if (!spf::noalloc_scratch_fits(sp_rs_bwd_workspace_bytes(desc))) return SP_ERR_WORKSPACE;
   void* scratch = nullptr;
   const sp_status_t st = scratch_for_current_device(&scratch);
   if (st != SP_OK) return st;
-  // Same validation and kernels as the workspace entry point; a problem whose
-  // partial rows need more than SP_NOALLOC_SCRATCH_BYTES is refused there
-  // with SP_ERR_WORKSPACE before anything is launched.
+  // Same validation and kernels as the workspace entry point.
   return sp_rs_dropout_residual_norm_bwd(desc, dy, dh_out, h_saved, gamma, mask, rstd, mean,
                                          d_residual, d_sum, dgamma, dbeta, scratch,
                                          (size_t)SP_NOALLOC_SCRATCH_BYTES, stream);

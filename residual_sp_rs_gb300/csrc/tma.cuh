@@ -1,8 +1,9 @@
 // tma.cuh -- bulk asynchronous copies (TMA, 1-D) and mbarriers, inline PTX.
 //
-// Every wait is bounded: after about kWaitNs (or kWaitLimit polls) the
-// waiter gives up and reports false, so a copy that never lands cannot hang
-// the GPU; the caller then marks its results invalid.  A waiting thread is
+// Every wait is bounded: after the caller's limit (kWaitNs unless a test
+// shortens it) or kWaitLimit polls the waiter gives up and reports false, so
+// a copy that never lands cannot hang the GPU; the caller then marks its
+// results invalid and reports the timeout in the device status word.  A waiting thread is
 // suspended by the hardware between polls, so waiters take no issue slots
 // from the warps that still work.
 #pragma once
@@ -71,15 +72,17 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after
+// `limit_ns` nanoseconds (or kWaitLimit polls) without it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  // the clock is read once per 64 polls: %globaltimer read in a tight loop
-  // on many SMs slows every reader of it
+  // the clock is read once per 64 polls (and on the first one): %globaltimer
+  // read in a tight loop on many SMs slows every reader of it
   const uint64_t t0 = global_ns();
+  const uint32_t suspend = limit_ns < kSuspendNs ? (uint32_t)limit_ns : kSuspendNs;
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
-    if ((i & 63u) == 63u && global_ns() - t0 > kWaitNs) return false;
+    if (mbar_try_wait_suspend(bar, parity, suspend)) return true;
+    if ((i & 63u) == 0u && global_ns() - t0 > limit_ns) return false;
   }
   return false;
 }

@@ -18,7 +18,7 @@ import os
 
 import torch
 
-from .build import LIB_PATH
+from .build import LIB_PATH, source_hash
 
 SP_F32, SP_BF16 = 0, 1
 SP_RMSNORM, SP_LAYERNORM = 0, 1
@@ -33,7 +33,7 @@ class SpRsDesc(ctypes.Structure):
                 ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("dtype", ctypes.c_int32),
                 ("norm", ctypes.c_int32), ("p", ctypes.c_float), ("eps", ctypes.c_float),
                 ("seed", ctypes.c_uint64), ("nshards", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32), ("status", ctypes.c_void_p)]
 
     @property
     def R(self) -> int:
@@ -47,8 +47,9 @@ class SpRsDesc(ctypes.Structure):
 class SpKernelPlan(ctypes.Structure):
     """Mirror of sp_kernel_plan_t (include/spfuse.h)."""
     _fields_ = [(n, ctypes.c_int32) for n in ("tma", "block", "nthr", "tpr", "vpt", "row_groups",
-                                              "rows_per_stage", "stages", "chunked", "reserved")] + \
-               [(n, ctypes.c_int64) for n in ("stage_bytes", "smem_bytes", "rows_per_cta", "ctas")]
+                                              "rows_per_stage", "stages", "chunked", "noalloc_fits")] + \
+               [(n, ctypes.c_int64) for n in ("stage_bytes", "smem_bytes", "rows_per_cta", "ctas",
+                                              "workspace_bytes")]
 
 
 class SpPlanInfo(ctypes.Structure):
@@ -56,10 +57,13 @@ class SpPlanInfo(ctypes.Structure):
     _fields_ = [("fwd", SpKernelPlan), ("bwd", SpKernelPlan)]
 
 
-def make_desc(T, j, S, B, H, dtype="bf16", norm="rms", p=0.0, eps=1e-6, seed=0, nshards=1):
+def make_desc(T, j, S, B, H, dtype="bf16", norm="rms", p=0.0, eps=1e-6, seed=0, nshards=1,
+              status=None):
+    """status: an int32/uint32 CUDA tensor of one element (the device status
+    word, see include/spfuse.h) or None."""
     return SpRsDesc(T=T, j=j, S=S, B=B, H=H, dtype=NAME_CODE.get(dtype, dtype),
                     norm=NORM_CODE.get(norm, norm), p=p, eps=eps, seed=int(seed) & (2**64 - 1),
-                    nshards=nshards, reserved=0)
+                    nshards=nshards, reserved=0, status=_ptr(status))
 
 
 _lib = None
@@ -74,6 +78,9 @@ def lib() -> ctypes.CDLL:
                 f"libspfuse.so is not built ({LIB_PATH}); run residual_sp_rs_gb300.build.build() "
                 "with the CUDA toolkit installed. There is no fallback implementation.")
         L = ctypes.CDLL(LIB_PATH)
+        L.sp_build_hash.restype = ctypes.c_char_p
+        L.sp_build_hash.argtypes = []
+        _verify_hash(L, source_hash())
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         D = ctypes.POINTER(SpRsDesc)
         L.sp_rs_dropout_residual_norm_fwd.restype = ctypes.c_int
@@ -97,6 +104,14 @@ def lib() -> ctypes.CDLL:
         L.sp_plan_describe.argtypes = [D, i32, i32, i32, i32, ctypes.POINTER(SpPlanInfo)]
         _lib = L
     return _lib
+
+
+def _verify_hash(L: ctypes.CDLL, expected: str) -> None:
+    """Refuse a library built from other sources than these."""
+    got = L.sp_build_hash().decode()
+    if got != expected:
+        raise RuntimeError(f"libspfuse.so is stale: built from sources {got[:12]}, the tree is "
+                           f"{expected[:12]}; rebuild it with residual_sp_rs_gb300.build.build()")
 
 
 def _ptr(t):
@@ -135,7 +150,7 @@ def sp_plan_describe(desc: SpRsDesc, sms: int, smem_optin: int, has_dh: bool = T
     out = {}
     for k in ("fwd", "bwd"):
         kp = getattr(info, k)
-        out[k] = {n: getattr(kp, n) for n, _ in SpKernelPlan._fields_ if n != "reserved"}
+        out[k] = {n: getattr(kp, n) for n, _ in SpKernelPlan._fields_}
     return out
 
 

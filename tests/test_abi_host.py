@@ -46,16 +46,26 @@ def test_library_exports_every_declared_symbol(spf):
             assert n in exported, n
 
 
-def test_library_is_built_for_sm_103a(spf):
-    out = subprocess.run(["cuobjdump", "--list-elf", spf.LIB_PATH], capture_output=True, text=True)
-    if out.returncode != 0:
-        pytest.skip("cuobjdump unavailable")
-    assert "sm_103a" in out.stdout
+def test_library_is_built_for_sm_103a_only():
+    from residual_sp_rs_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_library_matches_the_sources(spf):
+    """The library reports the hash of the sources it was built from, and the
+    binding refuses one whose hash is not the tree's."""
+    from residual_sp_rs_gb300 import build
+    L = spf.lib()
+    assert L.sp_build_hash().decode() == build.source_hash()
+    with pytest.raises(RuntimeError, match="stale"):
+        spf._verify_hash(L, "0" * 64)
 
 
 def test_struct_layout_matches_header(spf):
-    assert ctypes.sizeof(spf.SpRsDesc) == 64
+    assert ctypes.sizeof(spf.SpRsDesc) == 72
     assert spf.SpRsDesc.seed.offset == 48 and spf.SpRsDesc.nshards.offset == 56
+    assert spf.SpRsDesc.status.offset == 64
+    assert ctypes.sizeof(spf.SpKernelPlan) == 80 and spf.SpKernelPlan.workspace_bytes.offset == 72
 
 
 def test_status_strings(spf):
@@ -101,6 +111,9 @@ def test_fwd_rejects_bad_pointers(spf):
     d0 = spf.make_desc(2, 0, 16, 2, 64, "bf16", "rms", 0.0, 1e-5)
     d0.reserved = 1
     assert _fwd(spf, d0) == 1
+    d1 = spf.make_desc(2, 0, 16, 2, 64, "bf16", "rms", 0.0, 1e-5)
+    d1.status = FAKE + 2                        # the status word must be 4-byte aligned
+    assert _fwd(spf, d1) == 3
 
 
 def test_empty_problem_launches_nothing(spf):

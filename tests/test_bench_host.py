@@ -65,3 +65,43 @@ def test_packed_block_views_share_one_aligned_buffer():
     # writing a view writes the one buffer that is copied
     views[1].fill_(1.5)
     assert torch.equal(flat[ends[1][0]:ends[1][1]].view(torch.float32), torch.full((7,), 1.5))
+
+
+def test_graph_steps_cover_the_timed_run_exactly():
+    for k in (1, 20, 97, 200, 512):
+        assert bench.graph_steps(k) == k
+    for k in (1000, 50000, 4096):
+        g = bench.graph_steps(k)
+        assert k % g == 0 and 16 <= g <= bench.MAX_GRAPH_STEPS
+
+
+def test_graph_rotation_continues_across_replays():
+    """Replaying the graph variants in turn walks the sets in order, so every
+    set is reused only after all the others (the L2 rule holds across the
+    replay boundaries), and there are at least the sets the rule needs."""
+    for g, need in ((20, 23), (200, 23), (256, 23), (5, 2), (97, 23), (512, 3)):
+        n, variants = bench.graph_rotation(g, need)
+        assert n >= need
+        seq = []
+        for rep in range(3 * variants):
+            v = rep % variants
+            seq += [((v * g) % n + i) % n for i in range(g)]
+        assert seq == [i % n for i in range(len(seq))], (g, need)
+
+
+def test_timed_runs_reach_the_minimum_span():
+    durations = iter([10.0] * 100)
+    runs = bench.timed_runs(lambda: next(durations), min_ms=50.0, min_runs=3)
+    assert len(runs) == 5 and sum(runs) >= 50.0
+    runs = bench.timed_runs(lambda: 100.0, min_ms=50.0, min_runs=3)
+    assert len(runs) == 3
+
+
+def test_ranks_own_their_sequence_shard():
+    # one GPU plays the whole tensor-parallel group
+    assert bench.tp_dp_rank(0, 1, 2) == (0, 2, 0)
+    # N ranks: rank r is tensor-parallel rank r % T of replica r // T
+    got = [bench.tp_dp_rank(r, 8, 2) for r in range(8)]
+    assert got == [(r % 2, 1, r // 2) for r in range(8)]
+    shards = {(dp, j) for j, _, dp in got}
+    assert len(shards) == 8   # every (replica, shard) pair exactly once

@@ -21,8 +21,11 @@ def spf():
     return ops
 
 
-def _plans(spf, T, S, B, H, norm, nshards=1, has_dh=True, has_mask=True, sms=SMS, optin=OPTIN):
-    d = spf.make_desc(T, 0, S, B, H, "bf16", norm, 0.1, 1e-5, 0, nshards)
+NOALLOC_SCRATCH = 8 << 20  # SP_NOALLOC_SCRATCH_BYTES
+
+
+def _plans(spf, T, S, B, H, norm, nshards=1, has_dh=True, has_mask=True, sms=SMS, optin=OPTIN, p=0.1):
+    d = spf.make_desc(T, 0, S, B, H, "bf16", norm, p, 1e-5, 0, nshards)
     return spf.sp_plan_describe(d, sms, optin, has_dh, has_mask)
 
 
@@ -71,6 +74,9 @@ def _check_bwd(b, H, ln, rows, has_dh, has_mask, sms=SMS, max_smem=MAX_SMEM):
     ns = 2 if ln else 1
     assert b["stages"] * b["stage_bytes"] >= b["row_groups"] * ns * 8 * (nvec + 4) * 4
     assert b["ctas"] <= sms and b["ctas"] * b["rows_per_cta"] >= rows
+    # one fp32 partial row per CTA (and statistic)
+    assert b["workspace_bytes"] == min(max(rows, 1), sms) * H * 4 * ns
+    assert b["noalloc_fits"] == (1 if b["workspace_bytes"] <= NOALLOC_SCRATCH else 0)
 
 
 SHAPES = list(itertools.product(
@@ -140,6 +146,42 @@ def test_f32_runs_the_register_kernels(spf):
     d = spf.make_desc(2, 0, 16, 2, 64, "f32", "rms", 0.1, 1e-6, 0, 1)
     pl = spf.sp_plan_describe(d, SMS, OPTIN)
     assert pl["fwd"]["tma"] == 0 and pl["bwd"]["tma"] == 0
+
+
+def test_noalloc_scratch_covers_this_device_and_refuses_larger_ones(spf):
+    """The allocation-free backward refuses a problem whose partial rows do
+    not fit its fixed 8 MiB array.  On a 152-SM device no TMA-fed backward
+    gets there (at most 152 rows of H = 4096 x 2 statistics, or H = 8192 x 1:
+    5 MB); a device with twice the SMs would be refused the GPT LayerNorm
+    backward."""
+    most = 0
+    for T, SB, H, norm in SHAPES:
+        S, B = SB
+        b = _plans(spf, T, S, B, H, norm, T)["bwd"]
+        if b["tma"]:
+            assert b["noalloc_fits"] == 1
+            most = max(most, b["workspace_bytes"])
+    assert most == 152 * 4096 * 4 * 2
+    b = _plans(spf, 8, 4096, 1, 4096, "ln", 8, sms=304)["bwd"]
+    assert b["tma"] and b["workspace_bytes"] == 304 * 4096 * 8 > NOALLOC_SCRATCH
+    assert b["noalloc_fits"] == 0
+    b = _plans(spf, 8, 4096, 1, 4096, "rms", 8, sms=304)["bwd"]
+    assert b["workspace_bytes"] == 304 * 4096 * 4 and b["noalloc_fits"] == 1
+
+
+def test_describe_matches_what_the_calls_launch(spf):
+    # no rows: the forward launches nothing
+    pl = _plans(spf, 2, 0, 2, 768, "rms", 2)
+    assert all(v == 0 for v in pl["fwd"].values())
+    # p = 0: the backward reads no mask even when one is passed
+    with_p0 = _plans(spf, 2, 2048, 2, 768, "rms", 2, has_mask=True, p=0.0)["bwd"]
+    no_mask = _plans(spf, 2, 2048, 2, 768, "rms", 2, has_mask=False)["bwd"]
+    assert with_p0["stage_bytes"] == no_mask["stage_bytes"] == -(-no_mask["rows_per_stage"] * 3 * 2 * 768 // 16) * 16
+    # an opt-in limit below the kernels' static shared memory leaves no room
+    # for a ring: no TMA-fed plan (and no wrapped-around size)
+    for optin in (1, 512, STATIC_SMEM):
+        pl = _plans(spf, 2, 2048, 2, 768, "rms", 2, optin=optin)
+        assert pl["fwd"]["tma"] == 0 and pl["bwd"]["tma"] == 0
 
 
 def test_bad_limits_are_rejected(spf):

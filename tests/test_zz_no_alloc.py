@@ -5,19 +5,20 @@ device memory where they run the backward (allocator callbacks, frameworks
 whose caching allocator owns the device memory, paths that must not risk the
 device synchronisation of cudaMalloc/cudaFree).  It keeps its partial rows in
 a fixed array inside the library instead of a caller workspace.  This test
-checks its outputs against the workspace entry point's on two calls in a
-row, with different inputs, so leftovers of the first call in the shared
-array cannot leak into the second.  The file name sorts last so that a run
+checks that its outputs are bit-identical to the workspace entry point's
+(the same kernels on the same inputs) on two calls in a row, with different
+inputs, so leftovers of the first call in the shared array cannot leak into
+the second.  Its refusal of problems larger than the array is host
+arithmetic, checked on the CPU (tests/test_plan_host.py): no problem on a
+152-SM device needs more than 5 MB.  The file name sorts last so that a run
 stopping at the first failure has already run every other test.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from residual_sp_rs_gb300 import ops, synthetic as syn
-from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -61,23 +62,7 @@ def test_noalloc_backward_matches_workspace_backward(lib, name):
             _p(out["dbeta"]), torch.cuda.current_stream().cuda_stream)
         assert code == 0, ops.status_string(code)
         torch.cuda.synchronize()
-        for k in ("d_res", "d_sum"):
-            exact = syn.to_storage(ref[k].double())
-            parity.check_bf16(k, syn.to_storage(out[k]), exact.reshape(rows, H))
-        parity.check_reduction("dgamma", out["dgamma"].cpu().numpy(), ref["dgamma"].double().cpu().numpy())
-        if ref["dbeta"] is not None:
-            parity.check_reduction("dbeta", out["dbeta"].cpu().numpy(), ref["dbeta"].double().cpu().numpy())
-
-
-def test_noalloc_refuses_problems_beyond_its_scratch(lib):
-    # H = 8192 LayerNorm over many rows needs more partial-row storage than the fixed array
-    desc = ops.make_desc(1, 0, 65536, 1, 8192, "bf16", "ln", 0.0, 1e-5, 0, 1)
-    need = ops.sp_rs_bwd_workspace_bytes(desc)
-    if need <= (8 << 20):
-        pytest.skip("this device needs no more than the fixed scratch for the largest row")
-    t = torch.zeros(16, device="cuda", dtype=torch.bfloat16)   # never touched: refused first
-    r = torch.ones(16, device="cuda")
-    code = lib.sp_rs_dropout_residual_norm_bwd_noalloc(
-        ctypes.byref(desc), _p(t), None, _p(t), _p(t), None, _p(r), _p(r), _p(t), _p(t), _p(r),
-        _p(r), torch.cuda.current_stream().cuda_stream)
-    assert code == 5   # SP_ERR_WORKSPACE
+        # the same kernels on the same inputs: bit-identical results
+        for k in ("d_res", "d_sum", "dgamma", "dbeta"):
+            if ref[k] is not None:
+                assert torch.equal(out[k], ref[k]), (call, k)
