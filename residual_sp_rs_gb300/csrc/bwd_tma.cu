@@ -64,10 +64,26 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
       L.stage_bytes = (L.off_mask + (has_mask ? (uint32_t)(rb * H) : 0u) + 15u) & ~15u;
       L.nrg = nrg;
       L.rb = rb;
+      // A row group waits for a stage by the parity of its ring slot's full
+      // barrier, which is only unambiguous when the slot's previous stage
+      // has landed.  So when slots are reused, every stage a group consumes
+      // must come back to a slot whose previous stage the same group
+      // consumed: the stages form `lanes` interleaved sequences (stage j to
+      // the groups of lane j % lanes; rows go to the groups round robin),
+      // and the ring holds a multiple of `lanes` stages.
+      int lanes = nrg, g = rb;
+      for (int a0 = nrg; g != 0;) {  // lanes = nrg / gcd(nrg, rb)
+        const int t = a0 % g;
+        a0 = g;
+        g = t;
+        if (g == 0) lanes = nrg / a0;
+      }
+      const int64_t nstage = (rows_per_cta + rb - 1) / rb;
       int nst = 0;
       for (int cand = kMaxStages; cand >= 2; --cand) {
         const size_t bars = 16 * (((size_t)2 * cand * 8 + 15) / 16);
-        if (bars + fixed_base + (size_t)cand * L.stage_bytes <= budget) {
+        const bool reuse = nstage > cand;
+        if ((!reuse || cand % lanes == 0) && bars + fixed_base + (size_t)cand * L.stage_bytes <= budget) {
           nst = cand;
           break;
         }

@@ -378,52 +378,54 @@ __global__ void __launch_bounds__(NTHR, 1) sp_bwd_tma_kernel(const BwdArgs a, co
   }
 
   // ---- dgamma/dbeta: row groups' column sums into the ring, added in order ---
-  // The ring holds them as [nrg][NS][EV][pitch], pitch = nvec + 4: element e
-  // of vector v (column v*EV + e) at e*pitch + v.  A warp's stores (fixed e,
-  // consecutive v) hit consecutive banks, and so do the reads of 32
-  // consecutive columns (the 8 elements of a vector 4 banks apart).
-  const int pitch = nvec + 4;
-  const size_t plane = (size_t)EV * pitch;  // floats per row group and statistic
+  // The ring holds them as [nrg][NS][H] fp32: each thread stores the 8
+  // columns of each of its vectors as two float4; then each thread adds one
+  // float4 of columns over the row groups in group order (all the group
+  // loads in flight before the adds) and writes it to the CTA's partial row.
   float* part = reinterpret_cast<float*>(stages);
   if (!producer) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lr + k * tpr;
       if (v < nvec) {
-        float* dst = part + (size_t)rg * NS * plane + v;
+        float e[2][8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float lo, hi;
-          f2_split(dg[k][q], lo, hi);
-          dst[(2 * q) * pitch] = lo;
-          dst[(2 * q + 1) * pitch] = hi;
-          if constexpr (LN) {
-            f2_split(db[k][q], lo, hi);
-            dst[plane + (2 * q) * pitch] = lo;
-            dst[plane + (2 * q + 1) * pitch] = hi;
-          }
+          f2_split(dg[k][q], e[0][2 * q], e[0][2 * q + 1]);
+          if constexpr (LN) f2_split(db[k][q], e[1][2 * q], e[1][2 * q + 1]);
+        }
+#pragma unroll
+        for (int st = 0; st < NS; ++st) {
+          float4* dst = reinterpret_cast<float4*>(part + ((size_t)rg * NS + st) * H + (size_t)v * EV);
+          dst[0] = make_float4(e[st][0], e[st][1], e[st][2], e[st][3]);
+          dst[1] = make_float4(e[st][4], e[st][5], e[st][6], e[st][7]);
         }
       }
     }
   }
   __syncthreads();
-  for (int st = 0; st < NS; ++st) {
-    float* dst = a.ws + ((int64_t)st * a.nparts + blockIdx.x) * H;
-    for (int c = threadIdx.x; c < H; c += blockDim.x) {
-      const float* src = part + st * plane + (size_t)(c & (EV - 1)) * pitch + (c / EV);
-      const size_t gstride = (size_t)NS * plane;
-      // row groups in order; the loads of 4 groups are issued before adding
-      float acc = src[0];
-      for (int g0 = 1; g0 < nrg; g0 += 4) {
-        float t[4];
+  const int n4 = NS * H / 4;  // float4 columns of both statistics
+  const size_t gstride4 = (size_t)NS * H / 4;
+  for (int c4 = threadIdx.x; c4 < n4; c4 += blockDim.x) {
+    const float4* src = reinterpret_cast<const float4*>(part) + c4;
+    float4 acc = src[0];
+    for (int g0 = 1; g0 < nrg; g0 += 8) {
+      float4 t[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) t[u] = g0 + u < nrg ? src[(size_t)(g0 + u) * gstride] : 0.f;
+      for (int u = 0; u < 8; ++u)
+        if (g0 + u < nrg) t[u] = src[(size_t)(g0 + u) * gstride4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (g0 + u < nrg) acc += t[u];
+      for (int u = 0; u < 8; ++u) {
+        if (g0 + u < nrg) {
+          acc.x += t[u].x;
+          acc.y += t[u].y;
+          acc.z += t[u].z;
+          acc.w += t[u].w;
+        }
       }
-      __stcg(dst + c, acc);
     }
+    const int st = (c4 * 4) / H, c = c4 * 4 - st * H;
+    __stcg(reinterpret_cast<float4*>(a.ws + ((int64_t)st * a.nparts + blockIdx.x) * H + c), acc);
   }
 }
 

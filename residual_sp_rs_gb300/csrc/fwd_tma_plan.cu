@@ -10,12 +10,27 @@ constexpr int kMaxStages = 48;
 // its T+1 copies moves at least this many bytes (up to one row per group)
 constexpr size_t kMinCopy = 8192;
 
-int ring_stages(size_t stage, size_t gb, size_t budget) {
+// The most stages of `stage` bytes that fit next to gamma/beta.  A row group
+// waits for a stage by the parity of its ring slot's full barrier, which is
+// only unambiguous when the slot's previous stage has landed; so when the
+// CTA's `nstage` stages reuse slots, the ring holds a multiple of `lanes`
+// stages, which brings every slot back to the row group that consumed its
+// previous stage.
+int ring_stages(size_t stage, size_t gb, size_t budget, int64_t nstage, int lanes) {
   for (int cand = kMaxStages; cand >= 2; --cand) {
     const size_t bars = 16 * (((size_t)2 * cand * 8 + 15) / 16);
-    if (bars + gb + (size_t)cand * stage <= budget) return cand;
+    if ((nstage <= cand || cand % lanes == 0) && bars + gb + (size_t)cand * stage <= budget) return cand;
   }
   return 0;
+}
+
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
 }
 }  // namespace
 
@@ -45,9 +60,12 @@ bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms
     if ((int64_t)nrg > rows_per_cta) nrg = (int)rows_per_cta;
     int rb = (int)((kMinCopy + rowb - 1) / rowb);
     rb = rb < 1 ? 1 : (rb > nrg ? nrg : rb);
+    // rows go to the row groups round robin: the groups of stage j recur
+    // every nrg / gcd(nrg, rb) stages
     int nst = 0;
     for (; rb >= 1; --rb) {
-      nst = ring_stages((size_t)rb * (T + 1) * rowb, gb, budget);
+      nst = ring_stages((size_t)rb * (T + 1) * rowb, gb, budget, (rows_per_cta + rb - 1) / rb,
+                        nrg / gcd_int(nrg, rb));
       if (nst >= 2) break;
     }
     bool chunked = false;
@@ -59,7 +77,9 @@ bool plan_fwd_tma(int64_t H, int T, bool ln, int max_smem, int64_t rows, int sms
       rb = 1;
       blk = (size_t)tpr * 16;
       stage = blk * (T + 1);
-      nst = ring_stages(stage, gb, budget);
+      // a row is vpt consecutive stages; row i belongs to group i % nrg (one
+      // group consumes every stage in order: no constraint)
+      nst = ring_stages(stage, gb, budget, rows_per_cta * vpt, nrg > 1 ? nrg * vpt : 1);
       if (nst < 2) return false;
       chunked = true;
     }

@@ -183,6 +183,27 @@ def test_fwd_p0_without_mask_is_exact_residual_add():
     parity.compare_fwd("bf16", "rms", g, orc, pr, _np(inp["gamma"]))
 
 
+def test_fwd_from_shard_rows_equals_full_tensor_call():
+    """A rank that holds only its shard's rows of each partial (after the
+    reduce-scatter's exchange) gets the same forward, bit for bit, as the
+    call that reads them out of the full tensors."""
+    from residual_sp_rs_gb300 import sp_exchange as ex
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    R, H = w.R, w.H
+    for j in range(w.T):
+        d = _desc(w, j)
+        ref = _gpu_fwd(w, inp, j)
+        blocks = torch.stack([p.view(-1, H)[j * R:(j + 1) * R] for p in inp["partials"]]).contiguous()
+        res = inp["residual"].view(-1, H)[j * R:(j + 1) * R]
+        out = {k: torch.empty_like(v) for k, v in ref.items() if v is not None}
+        ex.forward_from_shard_rows(d, blocks, res, inp["gamma"], None, out["h"], out["y"], out["mask"],
+                                   out["rstd"], None)
+        torch.cuda.synchronize()
+        for k in out:
+            assert torch.equal(out[k], ref[k]), (j, k)
+
+
 def test_fwd_empty_rows_is_a_no_op():
     w = syn.WORKLOADS["pages_rms_bf16"].with_(S=0)
     d = _desc(w, 0)
@@ -300,6 +321,9 @@ def test_bwd_large_hidden_sampled(p):
     # two 8-warp LayerNorm row groups in the 544-thread block, several rows
     # per CTA: ragged last slot, and no dropout
     (2, 128, 3, 2064, "bf16", "ln", 0.1), (2, 160, 2, 4096, "bf16", "ln", 0.0),
+    # RMSNorm rows of 256 threads and 3 vectors in the 544-thread block, an
+    # odd number of rows per CTA
+    (2, 400, 1, 5120, "bf16", "rms", 0.1), (3, 306, 1, 5120, "bf16", "rms", 0.2),
 ])
 def test_bwd_edge_shapes(case):
     T, S, B, H, dt, nm, p = case
@@ -443,6 +467,37 @@ def test_bitwise_deterministic_runs():
     for k, v in outs[0].items():
         if v is not None:
             assert torch.equal(v, outs[1][k]), k
+
+
+@pytest.mark.parametrize("name", ["gpt_ln_bf16", "pages_rms_bf16"])
+def test_back_to_back_launches_match_a_single_launch(name):
+    """Many forward and backward launches back to back on one stream (the
+    next kernel's CTAs start while the previous one drains, and the ring
+    slots of every CTA are reused many times) give, bit for bit, the results
+    of the same call made alone."""
+    w = syn.WORKLOADS[name]
+    d = _desc(w, 0, w.T)
+    rows, H = d.rows, w.H
+    ins = [syn.fwd_inputs(w, DEV, seed=w.input_seed + 31 * k) for k in range(2)]
+    grs = [syn.upstream_grads(w, DEV, seed=w.input_seed + 31 * k) for k in range(2)]
+
+    def run(k):
+        f = ops.forward(d, ins[k]["partials"], ins[k]["residual"].view(rows, H), ins[k]["gamma"],
+                        ins[k]["beta"])
+        b = ops.backward(d, grs[k]["dy"].view(rows, H), grs[k]["dh_out"].view(rows, H), f["h"],
+                         ins[k]["gamma"], f["mask"], f["rstd"], f["mean"])
+        return {**f, **b}
+
+    ref = []
+    for k in range(2):
+        ref.append(run(k))
+        torch.cuda.synchronize()
+    outs = [run(i % 2) for i in range(24)]
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        for key, v in o.items():
+            if v is not None:
+                assert torch.equal(v, ref[i % 2][key]), (i, key)
 
 
 def test_outputs_stay_inside_their_buffers():

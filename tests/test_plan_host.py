@@ -2,6 +2,7 @@
 GPU): invariants that the TMA-fed kernels rely on, checked over a grid of
 shapes, and the configurations the three benchmark workloads run with."""
 import itertools
+import math
 
 import pytest
 
@@ -50,6 +51,14 @@ def _check_fwd(f, T, H, rows, sms=SMS, max_smem=MAX_SMEM):
         assert f["stage_bytes"] == f["rows_per_stage"] * 2 * H * (T + 1)
     assert f["ctas"] <= sms and f["ctas"] * f["rows_per_cta"] >= rows
     assert (f["ctas"] - 1) * f["rows_per_cta"] < rows
+    # when ring slots are reused, a slot always returns to the row group that
+    # consumed its previous stage (rows go to the groups round robin)
+    per_row = f["vpt"] if f["chunked"] else 1
+    nstage = -(-f["rows_per_cta"] // f["rows_per_stage"]) * per_row
+    if nstage > f["stages"] and f["row_groups"] > 1:
+        g = f["row_groups"]
+        lanes = g * per_row if f["chunked"] else g // math.gcd(g, f["rows_per_stage"])
+        assert f["stages"] % lanes == 0
 
 
 def _check_bwd(b, H, ln, rows, has_dh, has_mask, sms=SMS, max_smem=MAX_SMEM):
@@ -61,7 +70,15 @@ def _check_bwd(b, H, ln, rows, has_dh, has_mask, sms=SMS, max_smem=MAX_SMEM):
     if b["nthr"] == 544:
         # two 8-warp row groups, where the 16-warp block would hold one
         assert b["tpr"] == 256 and b["row_groups"] == 2 and b["vpt"] <= 3
-    else:
+    # rows go to the row groups round robin: the groups of a stage recur
+    # every `lanes` stages
+    lanes = b["row_groups"] // math.gcd(b["row_groups"], b["rows_per_stage"])
+    # when ring slots are reused, a slot always returns to the group(s) that
+    # consumed its previous stage, so a wait by barrier parity cannot match
+    # a phase two behind
+    if -(-b["rows_per_cta"] // b["rows_per_stage"]) > b["stages"]:
+        assert b["stages"] % lanes == 0
+    if b["nthr"] == 512:
         # the 16-warp block walks the ring stage by stage: rows per stage
         # divide the row groups
         assert b["row_groups"] % b["rows_per_stage"] == 0

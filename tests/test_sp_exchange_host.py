@@ -1,0 +1,87 @@
+"""The cross-rank exchange steps of sequence parallelism on CPU gloo ranks
+(world size 2 and 4): the reduce-scatter's exchange half, the norm-weight
+gradient all-reduce and the all-gather of the partials' gradient, checked
+against the oracle's simulated collectives (MiniMind-tron ch.3, §3.2.1,
+§3.2.3, §3.3.3.1, §3.4.2.1)."""
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _partial(t, S, B, H):
+    g = torch.Generator().manual_seed(100 + t)
+    return torch.randint(-8, 9, (S, B, H), generator=g).to(torch.float64) / 4
+
+
+def _rank(rank, world, port, q, S, B, H):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from residual_sp_rs_gb300 import sp_exchange as ex
+    blocks = ex.exchange_partials(_partial(rank, S, B, H))
+    dg = torch.arange(H, dtype=torch.float64) * (rank + 1)
+    db = torch.ones(H, dtype=torch.float64) * (rank + 1)
+    ex.allreduce_norm_grads(dg, db)
+    d_sum = torch.full(((S // world) * B, H), float(rank), dtype=torch.float64)
+    grads = ex.gather_partial_grads(d_sum)
+    q.put((rank, blocks.numpy(), dg.numpy(), db.numpy(), grads.numpy()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_exchange_allreduce_and_gather_on_gloo_ranks(world):
+    import oracle
+    S, B, H = 4 * world, 2, 8
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, q, S, B, H)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = sorted([q.get(timeout=180) for _ in range(world)], key=lambda x: x[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    P = [_partial(t, S, B, H).numpy() for t in range(world)]
+    R = (S // world) * B
+    for j, blocks, dg, db, grads in got:
+        # block t = rank t's rows of shard j; their rank-order sum is the
+        # reduce-scatter's shard j (the oracle's simulated collective)
+        for t in range(world):
+            assert np.array_equal(blocks[t], P[t].reshape(-1, H)[j * R:(j + 1) * R])
+        rs = oracle.reduce_scatter([p.ravel() for p in P], j)
+        assert np.array_equal(blocks.sum(axis=0).ravel(), rs)
+        # every rank holds the sum over ranks of the per-shard partials
+        exp_g = oracle.all_reduce([np.arange(H) * (r + 1.0) for r in range(world)])
+        exp_b = oracle.all_reduce([np.ones(H) * (r + 1.0) for r in range(world)])
+        assert np.array_equal(dg, exp_g) and np.array_equal(db, exp_b)
+        # the gradient of every partial: the ranks' d_sum shards in rank order
+        assert np.array_equal(grads, np.repeat(np.arange(world, dtype=np.float64), R)[:, None] * np.ones(H))
+    # the exchange moves (T-1)/T of a partial per rank, as the ring reduce-scatter
+    _, sent = oracle.ring_reduce_scatter([p.ravel() for p in P])
+    per_rank = (world - 1) * R * H
+    assert all(int(s) == per_rank for s in sent)
+
+
+def test_shard_row_addressing_rejects_mismatched_blocks():
+    sys.path.insert(0, ROOT)
+    from residual_sp_rs_gb300 import ops, sp_exchange as ex
+    d = ops.make_desc(2, 1, 8, 2, 16, "bf16", "rms", 0.1, 1e-6, 0)
+    with pytest.raises(ValueError):
+        ex.forward_from_shard_rows(d, torch.zeros(2, 4, 16, dtype=torch.bfloat16), None, None, None,
+                                   None, None, None, None, None)
