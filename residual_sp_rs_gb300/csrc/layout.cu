@@ -8,9 +8,13 @@
 // sp2hp walks the INPUT in order (coalesced reads; a warp's writes stay
 // inside one destination chunk of H/T elements except at chunk edges);
 // hp2sp walks the OUTPUT in order.  Index math is 32-bit when the vector
-// count allows it.
+// count allows it.  Before the grid-dependency wait, thread 0 of each CTA
+// starts bringing the CTA's input bytes into L2 (a hint: the loads after the
+// wait read whatever the previous kernel wrote), so in a stream the reads
+// overlap the previous kernel's tail.
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace spf {
 
@@ -24,9 +28,22 @@ template <bool TO_HP, typename Idx>
 __global__ void __launch_bounds__(kLayoutThreads)
     sp_layout_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, Idx total, Idx N,
                      Idx nv, Idx ncv) {
+  const Idx first = (Idx)blockIdx.x * (kLayoutThreads * kLayoutVPT);  // this CTA's walk
+  if (threadIdx.x == 0) {
+    const Idx last = min(total, first + (Idx)(kLayoutThreads * kLayoutVPT));  // exclusive
+    if (TO_HP) {
+      l2_prefetch(in + first, (uint32_t)((last - first) * 16));
+    } else {
+      // the rows n0..n1 of each rank's plane r: (r*N + n)*ncv .. + ncv
+      const Idx n0 = first / nv, n1 = (last - 1) / nv;
+      const Idx T = nv / ncv;
+      for (Idx r = 0; r < T; ++r)
+        l2_prefetch(in + (r * N + n0) * ncv, (uint32_t)((n1 - n0 + 1) * ncv * 16));
+    }
+  }
   grid_dep_wait();
   grid_dep_launch_dependents();
-  const Idx base = (Idx)blockIdx.x * (kLayoutThreads * kLayoutVPT) + threadIdx.x;
+  const Idx base = first + threadIdx.x;
   uint4 buf[kLayoutVPT];
   Idx dst[kLayoutVPT];
 #pragma unroll
