@@ -72,9 +72,9 @@ __device__ __forceinline__ uint32_t keep_bits4(uint64_t q, const PhiloxKeys& k, 
 
 // ---------------------------------------------------------------------------
 // 16-byte global accesses.  Inputs that are read once (partials, residual,
-// upstream gradients, saved activations) and all outputs use the streaming
-// (evict-first) cache policy; gamma/beta, re-read by every row, go through
-// the read-only path.
+// upstream gradients, saved activations) and the outputs read later use the
+// streaming (evict-first) cache policy; gamma/beta, re-read by every row, go
+// through the read-only path.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
@@ -84,6 +84,12 @@ __device__ __forceinline__ uint4 ld_cached(const void* p) {
 }
 __device__ __forceinline__ void st_stream(void* p, uint4 v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
+}
+// An output the next kernel reads right away (the norm output y, which the
+// sp2hp layout or the next GEMM reads next) is stored with the default
+// policy, so it stays in L2 for that reader.
+__device__ __forceinline__ void st_keep(void* p, uint4 v) {
+  *reinterpret_cast<uint4*>(p) = v;
 }
 
 // ---------------------------------------------------------------------------

@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(512) sp_fwd_kernel(const FwdArgs a) {
         }
         yout = V::pack(yv);
       }
-      st_stream(reinterpret_cast<Act*>(a.y) + r * (int64_t)a.H + (int64_t)v * EV, yout);
+      st_keep(reinterpret_cast<Act*>(a.y) + r * (int64_t)a.H + (int64_t)v * EV, yout);
     }
   }
   if (lr == 0) {
