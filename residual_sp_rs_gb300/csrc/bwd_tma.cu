@@ -45,7 +45,6 @@ bool plan_bwd_tma(int64_t H, bool ln, bool has_dh, bool has_mask, int max_smem, 
   const uint32_t rowb = (uint32_t)H * 2;
   const size_t fixed_base = (size_t)H * 4;  // gamma, fp32
   if (max_smem <= (int)kStaticSmem) return false;  // no room for a ring at all
-  if (max_smem <= (int)kStaticSmem) return false;  // no room for a ring at all
   const size_t budget = (size_t)max_smem - kStaticSmem;
   for (; nrg >= 1; --nrg) {
     const bool narrow = nrg * tpr + 32 <= kBwdTmaNarrow;
