@@ -56,6 +56,8 @@ def forward_from_shard_rows(desc, blocks: torch.Tensor, residual, gamma, beta, h
     T, R, H = blocks.shape
     if desc.T != T or desc.H != H or desc.R != R or max(1, desc.nshards) != 1:
         raise ValueError("blocks do not match the descriptor's single shard")
+    if not blocks.is_contiguous():
+        raise ValueError("blocks must be contiguous: each block is passed by its base address")
     row_bytes = H * blocks.element_size()
     base = [blocks[t].data_ptr() - desc.j * R * row_bytes for t in range(T)]
     ops.sp_rs_dropout_residual_norm_fwd(desc, base, residual, gamma, beta, h_out, y_out, mask_out,

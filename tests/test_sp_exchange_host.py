@@ -85,3 +85,8 @@ def test_shard_row_addressing_rejects_mismatched_blocks():
     with pytest.raises(ValueError):
         ex.forward_from_shard_rows(d, torch.zeros(2, 4, 16, dtype=torch.bfloat16), None, None, None,
                                    None, None, None, None, None)
+    # right shape, but a strided view: the blocks' base addresses would not hold its rows
+    strided = torch.zeros(8, 2, 16, dtype=torch.bfloat16).transpose(0, 1)
+    assert strided.shape == (2, 8, 16) and not strided.is_contiguous()
+    with pytest.raises(ValueError):
+        ex.forward_from_shard_rows(d, strided, None, None, None, None, None, None, None, None)
