@@ -133,6 +133,34 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc,
                                             float* rstd_out, float* mean_out,
                                             sp_stream_t stream);
 
+/* The forward above restricted to rows [row_begin, row_begin + row_count)
+ * of the call's nshards*R rows: the receiving side of a reduce-scatter split
+ * into pipeline chunks, where each chunk's reduction runs as soon as the
+ * chunk has arrived while the next chunks are still in flight ([SPN]
+ * communication-computation overlap, reduce-scatter overlap by pipeline
+ * chunks, 4 by default; [MT3] §3.2.3).  Every argument means what it means
+ * in sp_rs_dropout_residual_norm_fwd: residual, h_out, y_out, mask_out,
+ * rstd_out and mean_out address the call's row 0 and the partials are
+ * addressed by global row, so a caller that holds only a chunk's rows of
+ * partial t passes the address that chunk's rows imply for the partial's
+ * row 0 (the chunk buffer's address minus (j*R + row_begin)*H*element bytes).
+ * Only the rows of the range are read and written, and each of them comes
+ * out bit-identical to the full call's (the mask is keyed by the global
+ * element index).
+ * Errors: as the full call; besides, SP_ERR_INVALID_ARG unless
+ * 0 <= row_begin <= row_begin + row_count <= nshards*R, and SP_ERR_ALIGN when
+ * the range's first row breaks the 16-byte alignment of the activation or
+ * mask pointers (row_begin*H must be a multiple of 16 when a mask is
+ * stored).  row_count == 0 returns SP_OK without checking the pointers. */
+sp_status_t sp_rs_dropout_residual_norm_fwd_rows(const sp_rs_desc_t* desc,
+                                                 int64_t row_begin, int64_t row_count,
+                                                 const void* const* partials,
+                                                 const void* residual, const void* gamma,
+                                                 const void* beta, void* h_out, void* y_out,
+                                                 uint8_t* mask_out,
+                                                 float* rstd_out, float* mean_out,
+                                                 sp_stream_t stream);
+
 /* Bytes of device workspace sp_rs_dropout_residual_norm_bwd needs for this
  * problem on the CURRENT device (it depends on the SM count).  Returns 0 for
  * an invalid descriptor. */

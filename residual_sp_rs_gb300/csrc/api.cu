@@ -182,30 +182,39 @@ sp_status_t plan_bwd(const Problem& pr, bool has_dh, bool has_mask, BwdPlan* pl)
   return SP_OK;
 }
 
-
-}  // namespace
-}  // namespace spf
-
-using namespace spf;
-
-extern "C" {
-
-sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void* const* partials,
-                                            const void* residual, const void* gamma,
-                                            const void* beta, void* h_out, void* y_out,
-                                            uint8_t* mask_out, float* rstd_out, float* mean_out,
-                                            sp_stream_t stream) {
+// The forward over rows [row_begin, row_begin + row_count) of the call's
+// nshards*R rows (all of them unless `ranged`).  Per-row arguments address
+// the call's row 0; the partials and the dropout mask follow the global row
+// index, so a range computes exactly what the full call computes there.
+sp_status_t fwd_impl(const sp_rs_desc_t* desc, bool ranged, int64_t row_begin, int64_t row_count,
+                     const void* const* partials, const void* residual, const void* gamma,
+                     const void* beta, void* h_out, void* y_out, uint8_t* mask_out,
+                     float* rstd_out, float* mean_out, sp_stream_t stream) {
   Problem pr;
   sp_status_t st = check_desc(desc, &pr);
   if (st != SP_OK) return st;
   const bool ln = pr.norm == SP_LAYERNORM;
-  if (pr.rows == 0) return SP_OK;  // nothing to read or write
+  if (!ranged) {
+    row_begin = 0;
+    row_count = pr.rows;
+  } else if (row_begin < 0 || row_count < 0 || row_begin > pr.rows || row_count > pr.rows - row_begin) {
+    return SP_ERR_INVALID_ARG;
+  }
+  if (row_count == 0) return SP_OK;  // nothing to read or write
   if (!partials || !residual || !gamma || !h_out || !y_out || !rstd_out) return SP_ERR_INVALID_ARG;
   if (ln && (!beta || !mean_out)) return SP_ERR_INVALID_ARG;
   for (int t = 0; t < pr.T; ++t) {
     if (!partials[t]) return SP_ERR_INVALID_ARG;
     if (!aligned(partials[t], 16)) return SP_ERR_ALIGN;
   }
+  // the range's first row of every per-row argument
+  const int64_t rowb = pr.H * elem_bytes(pr.dtype);
+  residual = static_cast<const char*>(residual) + row_begin * rowb;
+  h_out = static_cast<char*>(h_out) + row_begin * rowb;
+  y_out = static_cast<char*>(y_out) + row_begin * rowb;
+  if (mask_out) mask_out += row_begin * pr.H;
+  rstd_out += row_begin;
+  if (ln) mean_out += row_begin;
   if (!aligned(residual, 16) || !aligned(gamma, 16) || !aligned(h_out, 16) || !aligned(y_out, 16) ||
       (ln && !aligned(beta, 16)) || (mask_out && !aligned(mask_out, 16)) || !aligned(rstd_out, 4) ||
       (ln && !aligned(mean_out, 4)))
@@ -221,8 +230,8 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   a.mask = mask_out;
   a.rstd = rstd_out;
   a.mean = ln ? mean_out : nullptr;
-  a.rows = pr.rows;
-  a.grow0 = (int64_t)pr.j * pr.R;
+  a.rows = row_count;
+  a.grow0 = (int64_t)pr.j * pr.R + row_begin;
   a.H = (int32_t)pr.H;
   a.nvec = pr.nvec;
   a.thr = (uint32_t)std::floor((double)desc->p * 4294967296.0);
@@ -252,9 +261,9 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
       qe = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (qe != cudaSuccess) return from_cuda(qe);
     FwdTmaPlan tp;
-    if (plan_fwd_tma(pr.H, pr.T, ln, optin, pr.rows, sms, &tp)) {
+    if (plan_fwd_tma(pr.H, pr.T, ln, optin, row_count, sms, &tp)) {
       a.tpr = tp.shape.tpr;
-      const dim3 grid((unsigned)((pr.rows + tp.layout.rows_per_cta - 1) / tp.layout.rows_per_cta));
+      const dim3 grid((unsigned)((row_count + tp.layout.rows_per_cta - 1) / tp.layout.rows_per_cta));
       return from_cuda(ln ? launch_fwd_tma_ln(a, pr.T, tp, grid, cs)
                           : launch_fwd_tma_rms(a, pr.T, tp, grid, cs));
     }
@@ -262,13 +271,40 @@ sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void
   const RowShape s = row_shape(pr.nvec, fwd_vpt_cap(pr.T));
   a.tpr = s.tpr;
   const int rpc = s.block / s.tpr;
-  const dim3 grid((unsigned)((pr.rows + rpc - 1) / rpc));
+  const dim3 grid((unsigned)((row_count + rpc - 1) / rpc));
   cudaError_t e;
   if (pr.dtype == SP_BF16)
     e = ln ? launch_fwd_bf16_ln(a, pr.T, s, grid, cs) : launch_fwd_bf16_rms(a, pr.T, s, grid, cs);
   else
     e = ln ? launch_fwd_f32_ln(a, pr.T, s, grid, cs) : launch_fwd_f32_rms(a, pr.T, s, grid, cs);
   return from_cuda(e);
+}
+
+
+}  // namespace
+}  // namespace spf
+
+using namespace spf;
+
+extern "C" {
+
+sp_status_t sp_rs_dropout_residual_norm_fwd(const sp_rs_desc_t* desc, const void* const* partials,
+                                            const void* residual, const void* gamma,
+                                            const void* beta, void* h_out, void* y_out,
+                                            uint8_t* mask_out, float* rstd_out, float* mean_out,
+                                            sp_stream_t stream) {
+  return fwd_impl(desc, false, 0, 0, partials, residual, gamma, beta, h_out, y_out, mask_out, rstd_out,
+                  mean_out, stream);
+}
+
+sp_status_t sp_rs_dropout_residual_norm_fwd_rows(const sp_rs_desc_t* desc, int64_t row_begin,
+                                                 int64_t row_count, const void* const* partials,
+                                                 const void* residual, const void* gamma,
+                                                 const void* beta, void* h_out, void* y_out,
+                                                 uint8_t* mask_out, float* rstd_out, float* mean_out,
+                                                 sp_stream_t stream) {
+  return fwd_impl(desc, true, row_begin, row_count, partials, residual, gamma, beta, h_out, y_out,
+                  mask_out, rstd_out, mean_out, stream);
 }
 
 size_t sp_rs_bwd_workspace_bytes(const sp_rs_desc_t* desc) {

@@ -85,6 +85,9 @@ def lib() -> ctypes.CDLL:
         D = ctypes.POINTER(SpRsDesc)
         L.sp_rs_dropout_residual_norm_fwd.restype = ctypes.c_int
         L.sp_rs_dropout_residual_norm_fwd.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.sp_rs_dropout_residual_norm_fwd_rows.restype = ctypes.c_int
+        L.sp_rs_dropout_residual_norm_fwd_rows.argtypes = [D, i64, i64, vp, vp, vp, vp, vp, vp, vp,
+                                                           vp, vp, vp]
         L.sp_rs_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.sp_rs_bwd_workspace_bytes.argtypes = [D]
         L.sp_rs_dropout_residual_norm_bwd.restype = ctypes.c_int
@@ -166,6 +169,16 @@ def sp_rs_dropout_residual_norm_fwd(desc: SpRsDesc, partials, residual, gamma, b
     _check(lib().sp_rs_dropout_residual_norm_fwd(
         ctypes.byref(desc), arr, _ptr(residual), _ptr(gamma), _ptr(beta), _ptr(h_out),
         _ptr(y_out), _ptr(mask_out), _ptr(rstd_out), _ptr(mean_out), _stream(stream)))
+
+
+def sp_rs_dropout_residual_norm_fwd_rows(desc: SpRsDesc, row_begin: int, row_count: int, partials,
+                                         residual, gamma, beta, h_out, y_out, mask_out, rstd_out,
+                                         mean_out, stream=None) -> None:
+    arr = (ctypes.c_void_p * max(1, len(partials)))(*[_ptr(p) for p in partials])
+    _check(lib().sp_rs_dropout_residual_norm_fwd_rows(
+        ctypes.byref(desc), int(row_begin), int(row_count), arr, _ptr(residual), _ptr(gamma),
+        _ptr(beta), _ptr(h_out), _ptr(y_out), _ptr(mask_out), _ptr(rstd_out), _ptr(mean_out),
+        _stream(stream)))
 
 
 def sp_rs_bwd_workspace_bytes(desc: SpRsDesc) -> int:

@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["sp_rs_dropout_residual_norm_fwd", "sp_rs_bwd_workspace_bytes",
+    for n in ["sp_rs_dropout_residual_norm_fwd", "sp_rs_dropout_residual_norm_fwd_rows",
+              "sp_rs_bwd_workspace_bytes",
               "sp_rs_dropout_residual_norm_bwd", "sp2hp", "hp2sp", "sp_status_string", "sp_version"]:
         assert n in names
 
@@ -114,6 +115,31 @@ def test_fwd_rejects_bad_pointers(spf):
     d1 = spf.make_desc(2, 0, 16, 2, 64, "bf16", "rms", 0.0, 1e-5)
     d1.status = FAKE + 2                        # the status word must be 4-byte aligned
     assert _fwd(spf, d1) == 3
+
+
+def _fwd_rows(spf, desc, row_begin, row_count, partials=None, mask=FAKE, ptr=FAKE):
+    partials = [ptr] * desc.T if partials is None else partials
+    arr = (ctypes.c_void_p * max(1, len(partials)))(*partials)
+    return spf.lib().sp_rs_dropout_residual_norm_fwd_rows(
+        ctypes.byref(desc), row_begin, row_count, arr, ptr, ptr, ptr, ptr, ptr, mask, ptr, ptr, None)
+
+
+def test_fwd_rows_validates_the_range(spf):
+    # T=2, S=16, B=2: 16 rows in the call; H=24 bf16 (48-byte rows, 24-byte mask rows)
+    d = spf.make_desc(2, 0, 16, 2, 24, "bf16", "rms", 0.1, 1e-6)
+    for rb, rc in [(-1, 4), (0, -1), (17, 0), (10, 7), (1 << 62, 1 << 62)]:
+        assert _fwd_rows(spf, d, rb, rc) == 1, (rb, rc)
+    assert _fwd_rows(spf, d, 16, 0) == 0          # an empty range at the end
+    assert _fwd_rows(spf, d, 3, 0, ptr=0) == 0    # empty: no pointer is checked or touched
+    assert _fwd_rows(spf, d, 0, 4, ptr=0) == 1    # a real range needs its pointers
+    # the range's first mask row must stay 16-byte aligned: row 1 starts 24 bytes in
+    assert _fwd_rows(spf, d, 1, 4) == 3
+    assert _fwd_rows(spf, d, 1, 4, mask=0) in (0, 6)   # no stored mask: accepted (6 = no GPU)
+    assert _fwd_rows(spf, d, 2, 4) in (0, 6)           # row 2 starts 48 bytes in
+    # nshards = T: the range runs over both shards' rows
+    d2 = spf.make_desc(2, 0, 16, 2, 24, "bf16", "rms", 0.1, 1e-6, 0, 2)
+    assert _fwd_rows(spf, d2, 30, 3) == 1
+    assert _fwd_rows(spf, d2, 30, 2) in (0, 6)
 
 
 def test_empty_problem_launches_nothing(spf):

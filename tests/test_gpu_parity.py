@@ -204,6 +204,83 @@ def test_fwd_from_shard_rows_equals_full_tensor_call():
             assert torch.equal(out[k], ref[k]), (j, k)
 
 
+def _sentinel_like(ref):
+    """Outputs shaped like `ref`, filled with values no forward writes (-3.0; mask byte 7)."""
+    return {k: torch.full_like(v, 7 if v.dtype == torch.uint8 else -3.0) for k, v in ref.items()
+            if v is not None}
+
+
+def _fwd_rows_call(w, inp, d, j, b, count, out, partials=None):
+    R = w.R
+    res = inp["residual"].view(w.S * w.B, w.H)[j * R:]
+    ops.sp_rs_dropout_residual_norm_fwd_rows(d, b, count, inp["partials"] if partials is None else partials,
+                                             res, inp["gamma"], inp["beta"], out["h"], out["y"],
+                                             out["mask"], out["rstd"], out.get("mean"))
+
+
+@pytest.mark.parametrize("name,j,nshards,cuts", [
+    ("pages_rms_bf16", 0, 2, [0, 1, 1000, 2049, 4096]),   # crosses the shard boundary at 2048
+    ("gpt_ln_bf16", 3, 1, [0, 129, 130, 512]),
+    ("tiny_rms_f32", 1, 1, [0, 3, 11, 16]),
+])
+def test_fwd_rows_chunks_equal_the_full_call(name, j, nshards, cuts):
+    """The forward run chunk by chunk over row ranges (the receiving side of
+    a reduce-scatter in pipeline chunks) writes, bit for bit, what one call
+    over all the rows writes: the mask is keyed by the global element index."""
+    w = syn.WORKLOADS[name]
+    inp = syn.fwd_inputs(w, DEV)
+    ref = _gpu_fwd(w, inp, j, nshards)
+    d = _desc(w, j, nshards)
+    out = _sentinel_like(ref)
+    for b, e in zip(cuts[:-1], cuts[1:]):
+        _fwd_rows_call(w, inp, d, j, b, e - b, out)
+    torch.cuda.synchronize()
+    for k in out:
+        assert torch.equal(out[k], ref[k]), k
+
+
+def test_fwd_rows_writes_only_its_range():
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    ref = _gpu_fwd(w, inp, 1)
+    d = _desc(w, 1)
+    out = _sentinel_like(ref)
+    b, e = 700, 1301
+    _fwd_rows_call(w, inp, d, 1, b, e - b, out)
+    _fwd_rows_call(w, inp, d, 1, 5, 0, out)   # an empty range launches nothing
+    torch.cuda.synchronize()
+    blank = _sentinel_like(ref)
+    for k in out:
+        assert torch.equal(out[k][b:e], ref[k][b:e]), k
+        assert torch.equal(out[k][:b], blank[k][:b]) and torch.equal(out[k][e:], blank[k][e:]), k
+
+
+def test_pipelined_chunks_from_received_rows_equal_the_full_call():
+    """Rank j of the pipelined exchange, emulated on one GPU: its own partial
+    in place and each chunk's rows of the other partials in a chunk buffer,
+    passed by the addresses chunk_partial_bases derives."""
+    from residual_sp_rs_gb300 import sp_exchange as ex
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    R, H, T = w.R, w.H, w.T
+    for j in range(T):
+        ref = _gpu_fwd(w, inp, j)
+        d = _desc(w, j)
+        own = inp["partials"][j].view(-1, H)
+        out = _sentinel_like(ref)
+        bufs = []
+        for b, e in ex.chunk_bounds(R, H, 4):
+            buf = torch.empty((T, e - b, H), device=DEV, dtype=own.dtype)
+            for t in range(T):
+                if t != j:
+                    buf[t].copy_(inp["partials"][t].view(-1, H)[j * R + b:j * R + e])
+            bufs.append(buf)
+            _fwd_rows_call(w, inp, d, j, b, e - b, out, ex.chunk_partial_bases(own, buf, j, R, b))
+        torch.cuda.synchronize()
+        for k in out:
+            assert torch.equal(out[k], ref[k]), (j, k)
+
+
 def test_fwd_empty_rows_is_a_no_op():
     w = syn.WORKLOADS["pages_rms_bf16"].with_(S=0)
     d = _desc(w, 0)

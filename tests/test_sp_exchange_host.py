@@ -90,3 +90,86 @@ def test_shard_row_addressing_rejects_mismatched_blocks():
     assert strided.shape == (2, 8, 16) and not strided.is_contiguous()
     with pytest.raises(ValueError):
         ex.forward_from_shard_rows(d, strided, None, None, None, None, None, None, None, None)
+
+
+def _pipelined_rank(rank, world, port, q, S, B, H, chunks):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from residual_sp_rs_gb300 import sp_exchange as ex
+    R = (S // world) * B
+    own = _partial(rank, S, B, H).to(torch.float32).view(-1, H)
+    res, gam, bet = _norm_inputs(S, B, H)
+    pr = oracle.problem(world, rank, S, B, H, "f32", "ln", 0.25, 1e-5, 7)
+    bounds = ex.chunk_bounds(R, H, chunks)
+    recv, works = ex.pull_chunks(own, bounds)
+    outs = []
+    for (b, e), buf, ws in zip(bounds, recv, works):
+        for w in ws:
+            w.wait()
+        # the chunk's rows of every partial: this rank's own in place, the rest as received
+        rows = [own[rank * R + b:rank * R + e] if t == rank else buf[t] for t in range(world)]
+        grows = rank * R + b + np.arange(e - b)
+        outs.append(oracle.fwd_rows(pr, grows, [r.numpy() for r in rows], res[rank * R + b:rank * R + e].numpy(),
+                                    gam.numpy(), bet.numpy(), "f32"))
+    cat = {k: np.concatenate([o[k] for o in outs]) for k in ("h", "y", "mask", "rstd", "mean")}
+    q.put((rank, bounds, cat))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def _norm_inputs(S, B, H):
+    g = torch.Generator().manual_seed(5)
+    res = torch.randn(S * B, H, generator=g, dtype=torch.float32)
+    gam = 1 + 0.1 * torch.randn(H, generator=g, dtype=torch.float32)
+    bet = 0.1 * torch.randn(H, generator=g, dtype=torch.float32)
+    return res, gam, bet
+
+
+@pytest.mark.parametrize("world,chunks", [(2, 3), (4, 4)])
+def test_pipelined_exchange_feeds_each_chunk_its_rows(world, chunks):
+    """The exchange in pipeline chunks ("Sequence Parallel" notes,
+    communication-computation overlap: the reduce-scatter in chunks): each
+    chunk's forward, run on just the rows that chunk brought in, reproduces
+    the whole shard's forward (MiniMind-tron ch.3, §3.2.3)."""
+    import oracle
+    oracle.build()
+    S, B, H = 8 * world, 2, 24
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_pipelined_rank, args=(r, world, port, q, S, B, H, chunks))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    got = sorted([q.get(timeout=180) for _ in range(world)], key=lambda x: x[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    P = [_partial(t, S, B, H).to(torch.float32).numpy() for t in range(world)]
+    res, gam, bet = _norm_inputs(S, B, H)
+    R = (S // world) * B
+    for j, bounds, cat in got:
+        assert len(bounds) == chunks and bounds[0][0] == 0 and bounds[-1][1] == R
+        assert all(e0 == b1 for (_, e0), (b1, _) in zip(bounds[:-1], bounds[1:]))
+        pr = oracle.problem(world, j, S, B, H, "f32", "ln", 0.25, 1e-5, 7)
+        full = oracle.fwd(pr, P, res[j * R:(j + 1) * R].numpy(), gam.numpy(), bet.numpy(), "f32")
+        for k in ("h", "y", "mask", "rstd", "mean"):
+            assert np.array_equal(cat[k], full[k]), (j, k)
+
+
+def test_chunk_bounds_keep_mask_rows_aligned():
+    sys.path.insert(0, ROOT)
+    from residual_sp_rs_gb300 import sp_exchange as ex
+    for R in (0, 1, 3, 16, 17, 2048, 4097):
+        for H in (8, 24, 768, 4104):
+            for chunks in (1, 2, 4, 7):
+                b = ex.chunk_bounds(R, H, chunks)
+                assert len(b) <= chunks
+                assert [x for x, _ in b][:1] in ([], [0]) and (not b or b[-1][1] == R)
+                assert all(e0 == b1 for (_, e0), (b1, _) in zip(b[:-1], b[1:]))
+                assert all(e > s and (s * H) % 16 == 0 for s, e in b)
+    with pytest.raises(ValueError):
+        ex.chunk_bounds(4, 8, 0)
