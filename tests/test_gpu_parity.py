@@ -281,6 +281,67 @@ def test_pipelined_chunks_from_received_rows_equal_the_full_call():
             assert torch.equal(out[k], ref[k]), (j, k)
 
 
+def _near_midpoint_inputs(R2, H, p, seed=11):
+    """Seeded forward inputs for T = 2 whose kept elements put
+    E = residual + (P0 + P1)/(1 - p) within 40 fp32 ulps of a bf16 rounding
+    midpoint (P1 = 0, so the sum is P0 exactly): random bf16 candidates,
+    kept by the distance of fp32(E) to the midpoint of its bf16 interval.
+    Every 8th row instead nearly cancels against the residual
+    (|E| < 2^-12 |residual|)."""
+    rng = np.random.default_rng(seed)
+    n = R2 * H
+
+    def bf16(x):  # round float64 -> bf16 bits (to nearest even via fp32) and back
+        b = np.asarray(x, np.float32).view(np.uint32)
+        b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+        return b, (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    s = 1.0 / (1.0 - np.float64(np.float32(p)))
+    p0s, ress = [], []
+    need = n
+    while need > 0:
+        m = 1 << 20
+        b0, v0 = bf16(rng.standard_normal(m) * 2.0 ** rng.integers(-4, 5, m))
+        br, vr = bf16(rng.standard_normal(m) * 2.0 ** rng.integers(-4, 5, m))
+        e32 = (vr + v0 * s).astype(np.float32)
+        low = (e32.view(np.uint32) & 0xFFFF).astype(np.int64)
+        hit = (np.abs(low - 0x8000) <= 40) & (v0 != 0)
+        p0s.append(b0[hit][:need])
+        ress.append(br[hit][:need])
+        need -= int(hit.sum())
+    P0 = np.concatenate(p0s)[:n].reshape(R2, H)
+    RES = np.concatenate(ress)[:n].reshape(R2, H)
+    # cancellation rows: residual = -bf16(P0*s) (+ one bf16 step), so E is tiny
+    v0 = (P0[::8].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    bc, _ = bf16(-v0 * s)
+    bc = bc + (rng.integers(0, 2, bc.shape)).astype(np.uint16)
+    RES[::8] = bc
+    return P0, np.zeros_like(P0), RES
+
+
+def test_fwd_h_rounding_near_bf16_midpoints():
+    """h = residual + sum/(1-p) rounded once to bf16 must be the correctly
+    rounded value also where it lies within a few fp32 ulps of a bf16
+    rounding midpoint, and where the residual add cancels."""
+    T, S, B, H, p = 2, 32, 2, 768, 0.1
+    w = syn.WORKLOADS["pages_rms_bf16"].with_(S=S, B=B)
+    R2 = S * B
+    P0, P1, RES = _near_midpoint_inputs(R2, H, p)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(DEV)
+    gamma = torch.ones(H, device=DEV, dtype=torch.bfloat16)
+    inp = {"partials": [to_dev(P0), to_dev(P1)], "residual": to_dev(RES), "gamma": gamma, "beta": None}
+    d = _desc(w, 0, 2)
+    out = ops.forward(d, inp["partials"], inp["residual"], gamma, None)
+    torch.cuda.synchronize()
+    pr = _oracle_problem(w, 0, 2)
+    orc = oracle.fwd(pr, [P0, P1], RES, _np(gamma), None, "bf16")
+    g = _np(out["h"])
+    kept = orc["mask"] == 1
+    assert kept.mean() > 0.8
+    assert np.array_equal(g, orc["h"]), int((g != orc["h"]).sum())
+    assert np.array_equal(_np(out["mask"]), orc["mask"])
+
+
 def test_fwd_empty_rows_is_a_no_op():
     w = syn.WORKLOADS["pages_rms_bf16"].with_(S=0)
     d = _desc(w, 0)
