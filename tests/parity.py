@@ -141,3 +141,27 @@ def compare_fwd(dtype: str, norm: str, gpu: dict, orc: dict, pr, gamma, beta=Non
         tolm = 1e-5 * np.maximum(np.abs(mean_ref), 1.0 / rstd_ref)
         bad = np.abs(m_gpu - mean_ref) > tolm
         assert not bad.any(), f"mean: {bad.sum()} rows out of tolerance"
+
+
+def tie_inputs(rows: int, H: int, seed: int = 3):
+    """Seeded bf16 forward inputs (for p = 0.5, so 1/(1-p) = 2) whose every
+    kept element lands EXACTLY on a bf16 rounding midpoint: residual r with a
+    7-bit mantissa m in 1..126 (both neighbours in r's binade), P0 =
+    +-ulp(r)/4 and every other partial 0, so E = r +- ulp(r)/2.  Returns
+    (P0, R, tie) as uint16 bf16 bit patterns; tie is the round-half-to-even result (of the
+    neighbours m and m +- 1 of |r|, the even mantissa), the expected h of a
+    kept element (a dropped one keeps r)."""
+    rng = np.random.default_rng(seed)
+    shape = (rows, H)
+    neg = rng.integers(0, 2, shape).astype(np.uint32)
+    exp = rng.integers(-6, 7, shape).astype(np.int64)
+    mant = rng.integers(1, 127, shape).astype(np.uint32)
+    away = rng.integers(0, 2, shape).astype(np.uint32)       # does P0 move |E| up?
+    r = (neg << 15) | ((exp + 127).astype(np.uint32) << 7) | mant
+    p0_neg = neg ^ (1 - away)                                 # same sign as r: |E| grows
+    p0 = (p0_neg << 15) | ((exp - 9 + 127).astype(np.uint32) << 7)
+    k = np.where(away == 1, 1, -1)
+    m_out = np.where(mant % 2 == 0, mant.astype(np.int64), mant.astype(np.int64) + k).astype(np.uint32)
+    tie = (neg << 15) | ((exp + 127).astype(np.uint32) << 7) | m_out
+    u16 = lambda a: a.astype(np.uint16)
+    return u16(p0), u16(r), u16(tie)

@@ -342,6 +342,25 @@ def test_fwd_h_rounding_near_bf16_midpoints():
     assert np.array_equal(_np(out["mask"]), orc["mask"])
 
 
+@pytest.mark.parametrize("T,H", [(2, 768), (4, 12288), (2, 16384)])   # whole-row ring, column chunks, registers
+def test_fwd_exact_ties_round_half_to_even(T, H):
+    """Every kept element an exact bf16 midpoint (p = 0.5): h must be the
+    neighbour with the even mantissa in each forward kernel, as in the oracle."""
+    S, B = 4 * T, 2
+    w = syn.WORKLOADS["pages_rms_bf16"].with_(T=T, S=S, B=B, H=H, p=0.5, seed=5)
+    P0, R, tie = parity.tie_inputs(S * B, H, seed=H)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(DEV)
+    gamma = torch.ones(H, device=DEV, dtype=torch.bfloat16)
+    parts = [P0] + [np.zeros_like(P0)] * (T - 1)
+    out = ops.forward(_desc(w, 0, T), [to_dev(p) for p in parts], to_dev(R), gamma, None)
+    torch.cuda.synchronize()
+    orc = oracle.fwd(_oracle_problem(w, 0, T), parts, R, _np(gamma), None, "bf16")
+    kept = orc["mask"] == 1
+    assert np.array_equal(_np(out["mask"]), orc["mask"])
+    assert np.array_equal(orc["h"], np.where(kept, tie, R))
+    assert np.array_equal(_np(out["h"]), orc["h"]), int((_np(out["h"]) != orc["h"]).sum())
+
+
 def test_fwd_empty_rows_is_a_no_op():
     w = syn.WORKLOADS["pages_rms_bf16"].with_(S=0)
     d = _desc(w, 0)

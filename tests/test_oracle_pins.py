@@ -689,3 +689,19 @@ def test_oracle_rejects_invalid_problems():
                    None, "f32")
     with pytest.raises(ValueError):
         oracle.sp2hp(np.zeros((5, 8), np.float32), 2)
+
+
+def test_forward_ties_round_half_to_even():
+    """With p = 0.5 (1/(1-p) = 2) every kept element of these inputs sums to
+    an exact bf16 midpoint: the stored h is the neighbour with the even
+    mantissa (IEEE round-half-to-even), and a dropped element keeps its
+    residual."""
+    from tests import parity
+    T, S, B, H = 2, 6, 1, 64
+    P0, R, tie = parity.tie_inputs(S * B, H)
+    pr = oracle.problem(T, 0, S, B, H, "bf16", "rms", 0.5, 1e-6, 5, nshards=T)
+    gamma = np.full(H, 0x3F80, np.uint16)                    # 1.0
+    out = oracle.fwd(pr, [P0, np.zeros_like(P0)], R, gamma, None, "bf16")
+    kept = out["mask"] == 1
+    assert 0.3 < kept.mean() < 0.7
+    assert np.array_equal(out["h"], np.where(kept, tie, R))
