@@ -205,6 +205,36 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc,
                                             void* workspace, size_t workspace_bytes,
                                             sp_stream_t stream);
 
+/* The backward above restricted to rows [row_begin, row_begin + row_count)
+ * of the call's nshards*R rows, so that a rank can pass on each chunk of its
+ * shard's d_sum (the all-gather that is the backward of the reduce-scatter,
+ * [MT3] §3.3.3.1) while the next chunk is still being computed ([SPN]
+ * communication-computation overlap).  Every argument means what it means in
+ * sp_rs_dropout_residual_norm_bwd: the per-row arguments address the call's
+ * row 0, and only the rows of the range are read and written, each of them
+ * bit-identical to the full call's.  dgamma/dbeta receive the sums over the
+ * range's rows; with accumulate != 0 they are added to what dgamma/dbeta
+ * hold (in a fixed order, so the chunks of a shard run in sequence on one
+ * stream give a deterministic result that equals the full call's up to the
+ * grouping of the sum), else they replace it.  The workspace of the full
+ * call suffices for any range.
+ * Errors: as the full call; besides, SP_ERR_INVALID_ARG unless
+ * 0 <= row_begin <= row_begin + row_count <= nshards*R, and SP_ERR_ALIGN when
+ * the range's first row breaks the 16-byte alignment of the activation or
+ * mask pointers.  row_count == 0 writes zeros to dgamma/dbeta, or with
+ * accumulate != 0 launches nothing. */
+sp_status_t sp_rs_dropout_residual_norm_bwd_rows(const sp_rs_desc_t* desc,
+                                                 int64_t row_begin, int64_t row_count,
+                                                 int32_t accumulate,
+                                                 const void* dy, const void* dh_out,
+                                                 const void* h_saved, const void* gamma,
+                                                 const uint8_t* mask,
+                                                 const float* rstd, const float* mean,
+                                                 void* d_residual, void* d_sum,
+                                                 float* dgamma, float* dbeta,
+                                                 void* workspace, size_t workspace_bytes,
+                                                 sp_stream_t stream);
+
 /* Size of the fixed device scratch of sp_rs_dropout_residual_norm_bwd_noalloc. */
 #define SP_NOALLOC_SCRATCH_BYTES (8u << 20)
 

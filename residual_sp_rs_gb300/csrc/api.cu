@@ -280,6 +280,105 @@ sp_status_t fwd_impl(const sp_rs_desc_t* desc, bool ranged, int64_t row_begin, i
   return from_cuda(e);
 }
 
+// The backward over rows [row_begin, row_begin + row_count) of the call's
+// nshards*R rows (all of them unless `ranged`).  Per-row arguments address
+// the call's row 0; the regenerated mask follows the global row index.
+// dgamma/dbeta receive the range's sums, added to what they hold when
+// `accumulate` is set.
+sp_status_t bwd_impl(const sp_rs_desc_t* desc, bool ranged, int64_t row_begin, int64_t row_count,
+                     bool accumulate, const void* dy, const void* dh_out, const void* h_saved,
+                     const void* gamma, const uint8_t* mask, const float* rstd, const float* mean,
+                     void* d_residual, void* d_sum, float* dgamma, float* dbeta, void* workspace,
+                     size_t workspace_bytes, sp_stream_t stream) {
+  Problem pr;
+  sp_status_t st = check_desc(desc, &pr);
+  if (st != SP_OK) return st;
+  const bool ln = pr.norm == SP_LAYERNORM;
+  if (!ranged) {
+    row_begin = 0;
+    row_count = pr.rows;
+  } else if (row_begin < 0 || row_count < 0 || row_begin > pr.rows || row_count > pr.rows - row_begin) {
+    return SP_ERR_INVALID_ARG;
+  }
+  // with no rows only dgamma/dbeta are written (zeros, or left as they are
+  // when accumulating); the rest may be NULL
+  const bool empty = row_count == 0;
+  if (!dgamma || (ln && !dbeta)) return SP_ERR_INVALID_ARG;
+  if (!empty && (!dy || !h_saved || !gamma || !rstd || !d_residual || !d_sum))
+    return SP_ERR_INVALID_ARG;
+  if (!empty && ln && !mean) return SP_ERR_INVALID_ARG;
+  if (!empty) {  // the range's first row of every per-row argument
+    const int64_t rowb = pr.H * elem_bytes(pr.dtype);
+    dy = static_cast<const char*>(dy) + row_begin * rowb;
+    if (dh_out) dh_out = static_cast<const char*>(dh_out) + row_begin * rowb;
+    h_saved = static_cast<const char*>(h_saved) + row_begin * rowb;
+    if (mask) mask += row_begin * pr.H;
+    rstd += row_begin;
+    if (ln) mean += row_begin;
+    d_residual = static_cast<char*>(d_residual) + row_begin * rowb;
+    d_sum = static_cast<char*>(d_sum) + row_begin * rowb;
+  }
+  if (!aligned(dy, 16) || (dh_out && !aligned(dh_out, 16)) || !aligned(h_saved, 16) ||
+      !aligned(gamma, 16) || (mask && !aligned(mask, 16)) || !aligned(rstd, 4) ||
+      (ln && !aligned(mean, 4)) || !aligned(d_residual, 16) || !aligned(d_sum, 16) ||
+      !aligned(dgamma, 16) || (ln && !aligned(dbeta, 16)))
+    return SP_ERR_ALIGN;
+  if (empty && accumulate) return SP_OK;  // nothing to add, nothing launched
+  Problem prr = pr;  // the rows this call processes
+  prr.rows = row_count;
+  BwdPlan pl;
+  st = plan_bwd(prr, dh_out != nullptr, desc->p > 0.0f && mask != nullptr, &pl);
+  if (st != SP_OK) return st;
+  if (!workspace || workspace_bytes < pl.ws_bytes) return SP_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return SP_ERR_ALIGN;
+  if (inject_launch_failure()) return SP_ERR_CUDA;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  float* ws = static_cast<float*>(workspace);
+  int nparts = 0;
+  if (!empty) {
+    BwdArgs a = {};
+    a.dy = dy;
+    a.dh = dh_out;
+    a.h = h_saved;
+    a.gamma = gamma;
+    a.mask = desc->p > 0.0f ? mask : nullptr;
+    a.regen = desc->p > 0.0f && !mask ? 1 : 0;
+    a.thr = (uint32_t)std::floor((double)desc->p * 4294967296.0);
+    a.grow0 = (int64_t)pr.j * pr.R + row_begin;
+    for (int i = 0; i < 10; ++i) {
+      a.keys.rk[2 * i] = (uint32_t)desc->seed + (uint32_t)i * 0x9E3779B9u;
+      a.keys.rk[2 * i + 1] = (uint32_t)(desc->seed >> 32) + (uint32_t)i * 0xBB67AE85u;
+    }
+    a.rstd = rstd;
+    a.mean = ln ? mean : nullptr;
+    a.d_res = d_residual;
+    a.d_sum = d_sum;
+    a.ws = ws;
+    a.rows = row_count;
+    a.rows_per_cta = pl.rows_per_cta;
+    a.H = (int32_t)pr.H;
+    a.nvec = pr.nvec;
+    a.tpr = pl.shape.tpr;
+    a.nparts = pl.nparts;
+    a.scale = (float)(1.0 / (1.0 - (double)desc->p));
+    a.Hf = (float)pr.H;
+    a.status = desc->status;
+    a.wait_ns = wait_hooks().wait_ns;
+    a.drop_stage = wait_hooks().drop_stage;
+    cudaError_t e;
+    if (pl.tma) {
+      a.tpr = pl.tp.shape.tpr;
+      e = launch_bwd_tma(ln, a, pl.tp, dim3((unsigned)pl.ctas), cs);
+    } else {
+      e = launch_bwd(pr.dtype, ln, a, pl.shape, dim3((unsigned)pl.ctas), pl.smem, cs);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    nparts = pl.nparts;
+  }
+  return from_cuda(launch_colsum(ws, nparts, (int)pr.H, ln, dgamma, ln ? dbeta : nullptr, accumulate, cs));
+}
+
 
 }  // namespace
 }  // namespace spf
@@ -322,72 +421,20 @@ sp_status_t sp_rs_dropout_residual_norm_bwd(const sp_rs_desc_t* desc, const void
                                             void* d_residual, void* d_sum, float* dgamma,
                                             float* dbeta, void* workspace, size_t workspace_bytes,
                                             sp_stream_t stream) {
-  Problem pr;
-  sp_status_t st = check_desc(desc, &pr);
-  if (st != SP_OK) return st;
-  const bool ln = pr.norm == SP_LAYERNORM;
-  // with no rows only dgamma/dbeta are written (zeros); the rest may be NULL
-  const bool empty = pr.rows == 0;
-  if (!dgamma || (ln && !dbeta)) return SP_ERR_INVALID_ARG;
-  if (!empty && (!dy || !h_saved || !gamma || !rstd || !d_residual || !d_sum))
-    return SP_ERR_INVALID_ARG;
-  if (!empty && ln && !mean) return SP_ERR_INVALID_ARG;
-  if (!aligned(dy, 16) || (dh_out && !aligned(dh_out, 16)) || !aligned(h_saved, 16) ||
-      !aligned(gamma, 16) || (mask && !aligned(mask, 16)) || !aligned(rstd, 4) ||
-      (ln && !aligned(mean, 4)) || !aligned(d_residual, 16) || !aligned(d_sum, 16) ||
-      !aligned(dgamma, 16) || (ln && !aligned(dbeta, 16)))
-    return SP_ERR_ALIGN;
-  BwdPlan pl;
-  st = plan_bwd(pr, dh_out != nullptr, desc->p > 0.0f && mask != nullptr, &pl);
-  if (st != SP_OK) return st;
-  if (!workspace || workspace_bytes < pl.ws_bytes) return SP_ERR_WORKSPACE;
-  if (!aligned(workspace, 16)) return SP_ERR_ALIGN;
-  if (inject_launch_failure()) return SP_ERR_CUDA;
+  return bwd_impl(desc, false, 0, 0, false, dy, dh_out, h_saved, gamma, mask, rstd, mean, d_residual,
+                  d_sum, dgamma, dbeta, workspace, workspace_bytes, stream);
+}
 
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  float* ws = static_cast<float*>(workspace);
-  int nparts = 0;
-  if (pr.rows > 0) {
-    BwdArgs a = {};
-    a.dy = dy;
-    a.dh = dh_out;
-    a.h = h_saved;
-    a.gamma = gamma;
-    a.mask = desc->p > 0.0f ? mask : nullptr;
-    a.regen = desc->p > 0.0f && !mask ? 1 : 0;
-    a.thr = (uint32_t)std::floor((double)desc->p * 4294967296.0);
-    a.grow0 = (int64_t)pr.j * pr.R;
-    for (int i = 0; i < 10; ++i) {
-      a.keys.rk[2 * i] = (uint32_t)desc->seed + (uint32_t)i * 0x9E3779B9u;
-      a.keys.rk[2 * i + 1] = (uint32_t)(desc->seed >> 32) + (uint32_t)i * 0xBB67AE85u;
-    }
-    a.rstd = rstd;
-    a.mean = ln ? mean : nullptr;
-    a.d_res = d_residual;
-    a.d_sum = d_sum;
-    a.ws = ws;
-    a.rows = pr.rows;
-    a.rows_per_cta = pl.rows_per_cta;
-    a.H = (int32_t)pr.H;
-    a.nvec = pr.nvec;
-    a.tpr = pl.shape.tpr;
-    a.nparts = pl.nparts;
-    a.scale = (float)(1.0 / (1.0 - (double)desc->p));
-    a.Hf = (float)pr.H;
-    a.status = desc->status;
-    a.wait_ns = wait_hooks().wait_ns;
-    a.drop_stage = wait_hooks().drop_stage;
-    cudaError_t e;
-    if (pl.tma) {
-      a.tpr = pl.tp.shape.tpr;
-      e = launch_bwd_tma(ln, a, pl.tp, dim3((unsigned)pl.ctas), cs);
-    } else {
-      e = launch_bwd(pr.dtype, ln, a, pl.shape, dim3((unsigned)pl.ctas), pl.smem, cs);
-    }
-    if (e != cudaSuccess) return from_cuda(e);
-    nparts = pl.nparts;
-  }
-  return from_cuda(launch_colsum(ws, nparts, (int)pr.H, ln, dgamma, ln ? dbeta : nullptr, cs));
+sp_status_t sp_rs_dropout_residual_norm_bwd_rows(const sp_rs_desc_t* desc, int64_t row_begin,
+                                                 int64_t row_count, int32_t accumulate,
+                                                 const void* dy, const void* dh_out,
+                                                 const void* h_saved, const void* gamma,
+                                                 const uint8_t* mask, const float* rstd,
+                                                 const float* mean, void* d_residual, void* d_sum,
+                                                 float* dgamma, float* dbeta, void* workspace,
+                                                 size_t workspace_bytes, sp_stream_t stream) {
+  return bwd_impl(desc, true, row_begin, row_count, accumulate != 0, dy, dh_out, h_saved, gamma, mask,
+                  rstd, mean, d_residual, d_sum, dgamma, dbeta, workspace, workspace_bytes, stream);
 }
 
 static sp_status_t layout_call(bool to_hp, const void* in, void* out, int64_t N, int64_t H,

@@ -54,10 +54,11 @@ cudaError_t launch_bwd(int dtype, bool ln, const BwdArgs& a, const RowShape& s, 
 }
 
 cudaError_t launch_colsum(const float* ws, int nparts, int H, bool ln, float* dgamma,
-                          float* dbeta, cudaStream_t st) {
+                          float* dbeta, bool accumulate, cudaStream_t st) {
   const int n4 = H / 4;
   const dim3 grid((unsigned)((n4 + 31) / 32), ln ? 2u : 1u);
-  return pdl_launch(sp_colsum_kernel, grid, dim3(32, 32), 0, st, ws, nparts, H, dgamma, dbeta);
+  return pdl_launch(sp_colsum_kernel, grid, dim3(32, 32), 0, st, ws, nparts, H, dgamma, dbeta,
+                    accumulate ? 1 : 0);
 }
 
 }  // namespace spf

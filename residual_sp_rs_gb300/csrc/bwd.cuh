@@ -198,9 +198,11 @@ __global__ void __cluster_dims__(kBwdCluster, 1, 1) __launch_bounds__(512)
 // group, y a stride class of partial rows (p = y, y+32, ...).  Each thread
 // issues all its loads (up to 8 per round) before adding, then the 32 stride
 // sums are added pairwise (y + 16, 8, 4, 2, 1).  The order is fixed, so the
-// result is bit-identical from run to run.
+// result is bit-identical from run to run.  With `accumulate` the sum is added
+// to what dgamma/dbeta hold (the earlier chunks of a row range), else it
+// replaces it.
 __global__ void __launch_bounds__(1024) sp_colsum_kernel(const float* ws, int nparts, int H,
-                                                         float* dgamma, float* dbeta) {
+                                                         float* dgamma, float* dbeta, int accumulate) {
   __shared__ float4 part[32][32];
   grid_dep_wait();
   grid_dep_launch_dependents();
@@ -242,7 +244,14 @@ __global__ void __launch_bounds__(1024) sp_colsum_kernel(const float* ws, int np
       part[threadIdx.y][threadIdx.x] = acc;
     }
   }
-  if (threadIdx.y == 0 && c4 < n4) reinterpret_cast<float4*>(dst)[c4] = acc;
+  if (threadIdx.y == 0 && c4 < n4) {
+    float4* d4 = reinterpret_cast<float4*>(dst) + c4;
+    if (accumulate) {
+      const float4 o = *d4;
+      acc = make_float4(o.x + acc.x, o.y + acc.y, o.z + acc.z, o.w + acc.w);
+    }
+    *d4 = acc;
+  }
 }
 
 }  // namespace spf

@@ -67,7 +67,7 @@ cudaError_t launch_bwd(int dtype, bool ln, const BwdArgs& a, const RowShape& s, 
                        size_t smem, cudaStream_t st);
 int bwd_max_active_clusters(int dtype, bool ln, const RowShape& s, size_t smem);
 cudaError_t launch_colsum(const float* ws, int nparts, int H, bool ln, float* dgamma,
-                          float* dbeta, cudaStream_t st);
+                          float* dbeta, bool accumulate, cudaStream_t st);
 
 // TMA-fed backward (bf16, H % 16 == 0): shared-memory ring layout and shape.
 // Block sizes the TMA backward is compiled for: 15 consumer warps + producer

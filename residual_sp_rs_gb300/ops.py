@@ -93,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.sp_rs_dropout_residual_norm_bwd.restype = ctypes.c_int
         L.sp_rs_dropout_residual_norm_bwd.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                       vp, vp, ctypes.c_size_t, vp]
+        L.sp_rs_dropout_residual_norm_bwd_rows.restype = ctypes.c_int
+        L.sp_rs_dropout_residual_norm_bwd_rows.argtypes = [D, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp,
+                                                           vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         for name in ("sp2hp", "hp2sp"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
@@ -194,6 +197,16 @@ def sp_rs_dropout_residual_norm_bwd(desc: SpRsDesc, dy, dh_out, h_saved, gamma, 
         ctypes.byref(desc), _ptr(dy), _ptr(dh_out), _ptr(h_saved), _ptr(gamma), _ptr(mask),
         _ptr(rstd), _ptr(mean), _ptr(d_residual), _ptr(d_sum), _ptr(dgamma), _ptr(dbeta),
         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def sp_rs_dropout_residual_norm_bwd_rows(desc: SpRsDesc, row_begin: int, row_count: int, accumulate: bool,
+                                         dy, dh_out, h_saved, gamma, mask, rstd, mean, d_residual, d_sum,
+                                         dgamma, dbeta, workspace, stream=None) -> None:
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().sp_rs_dropout_residual_norm_bwd_rows(
+        ctypes.byref(desc), int(row_begin), int(row_count), int(bool(accumulate)), _ptr(dy), _ptr(dh_out),
+        _ptr(h_saved), _ptr(gamma), _ptr(mask), _ptr(rstd), _ptr(mean), _ptr(d_residual), _ptr(d_sum),
+        _ptr(dgamma), _ptr(dbeta), _ptr(workspace), nbytes, _stream(stream)))
 
 
 def sp2hp(inp, out, N, H, T, dtype, stream=None) -> None:

@@ -22,6 +22,10 @@ communication around the fused kernels; all arithmetic stays in libspfuse:
   runs as soon as that chunk has landed, while the later chunks are still in
   flight.  A rank's own partial is read in place: only (T-1)/T of the shard's
   rows travel.
+* ``backward_pipelined``: the backward in the same chunks, each chunk's
+  d_sum all-gathered (``post_chunk_gather``) while the next chunk computes
+  (``sp_rs_dropout_residual_norm_bwd_rows``, dgamma/dbeta accumulated over
+  the chunks in order).
 * ``allreduce_norm_grads``: dgamma/dbeta are per-shard partial sums; the
   replicated norm weights need their sum over ranks (MiniMind-tron ch.3,
   §3.4.2.1).
@@ -150,11 +154,12 @@ def chunk_partial_bases(own: torch.Tensor, recv_chunk: torch.Tensor, j: int, R: 
 
 
 def forward_pipelined(desc, partial: torch.Tensor, residual, gamma, beta, h_out, y_out, mask_out,
-                      rstd_out, mean_out, chunks: int = 4, group=None, stream=None):
+                      rstd_out, mean_out, chunks: int = 4, group=None):
     """The fused forward of this rank's shard (desc.j = rank, desc.T = world
     size, one shard) from every rank's full partial, the exchange pipelined
-    in chunks.  Returns the chunk receive buffers: keep them alive until the
-    forward has run on the stream."""
+    in chunks.  The kernels go to the current stream, which each chunk's
+    transfers are ordered with.  Returns the chunk receive buffers: keep them
+    alive until the forward has run."""
     T = dist.get_world_size(group)
     j = dist.get_rank(group)
     H = partial.shape[-1]
@@ -169,5 +174,43 @@ def forward_pipelined(desc, partial: torch.Tensor, residual, gamma, beta, h_out,
             w.wait()
         ops.sp_rs_dropout_residual_norm_fwd_rows(desc, b, e - b, chunk_partial_bases(own, buf, j, R, b),
                                                  residual, gamma, beta, h_out, y_out, mask_out, rstd_out,
-                                                 mean_out, stream)
+                                                 mean_out)
     return recv
+
+
+def post_chunk_gather(d_sum: torch.Tensor, grad: torch.Tensor, R: int, b: int, e: int, group=None):
+    """Post the all-gather of rows [b, e) of this rank's d_sum shard ([R, H])
+    into rows [t*R + b, t*R + e) of grad ([T*R, H], the gradient of every
+    row-parallel partial) for every rank t.  Returns the work handle."""
+    T = dist.get_world_size(group)
+    outs = [grad[t * R + b:t * R + e] for t in range(T)]
+    return dist.all_gather(outs, d_sum[b:e], group=group, async_op=True)
+
+
+def backward_pipelined(desc, dy, dh_out, h_saved, gamma, mask, rstd, mean, d_residual, d_sum, dgamma,
+                       dbeta, workspace, chunks: int = 4, group=None):
+    """The fused backward of this rank's shard (desc.j = rank, desc.T = world
+    size, one shard) in pipeline chunks of its rows: as soon as a chunk's
+    d_sum rows are computed, their all-gather -- the backward of the
+    reduce-scatter (MiniMind-tron ch.3, §3.3.3.1) -- is posted, and it runs
+    while the next chunk is computed.  The chunks accumulate dgamma/dbeta in
+    order (this shard's sums; allreduce_norm_grads adds them over ranks).
+    The kernels go to the current stream.  Returns (grad, works): grad is the
+    [T*R, H] gradient of every row-parallel partial, complete once every work
+    handle has been waited on."""
+    T = dist.get_world_size(group)
+    j = dist.get_rank(group)
+    R, H = desc.R, desc.H
+    if desc.T != T or desc.j != j or max(1, desc.nshards) != 1:
+        raise ValueError("the descriptor must describe this rank's single shard")
+    bounds = chunk_bounds(R, H, chunks)
+    grad = torch.empty((T * R, H), dtype=d_sum.dtype, device=d_sum.device)
+    works = []
+    if not bounds:  # no rows: dgamma/dbeta are zeros
+        ops.sp_rs_dropout_residual_norm_bwd_rows(desc, 0, 0, False, dy, dh_out, h_saved, gamma, mask, rstd,
+                                                 mean, d_residual, d_sum, dgamma, dbeta, workspace)
+    for c, (b, e) in enumerate(bounds):
+        ops.sp_rs_dropout_residual_norm_bwd_rows(desc, b, e - b, c > 0, dy, dh_out, h_saved, gamma, mask, rstd,
+                                                 mean, d_residual, d_sum, dgamma, dbeta, workspace)
+        works.append(post_chunk_gather(d_sum, grad, R, b, e, group))
+    return grad, works

@@ -31,6 +31,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["sp_rs_dropout_residual_norm_fwd", "sp_rs_dropout_residual_norm_fwd_rows",
+              "sp_rs_dropout_residual_norm_bwd_rows",
               "sp_rs_bwd_workspace_bytes",
               "sp_rs_dropout_residual_norm_bwd", "sp2hp", "hp2sp", "sp_status_string", "sp_version"]:
         assert n in names
@@ -160,6 +161,24 @@ def test_bwd_rejects_bad_arguments(spf):
     bad = spf.make_desc(3, 0, 16, 2, 64, "bf16", "rms", 0.1, 1e-6)
     assert call(bad) == 2
     assert L.sp_rs_bwd_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+def test_bwd_rows_validates_the_range(spf):
+    L = spf.lib()
+    # T=2, S=16, B=2: 16 rows in the call; H=24 bf16 (48-byte rows, 24-byte mask rows)
+    d = spf.make_desc(2, 0, 16, 2, 24, "bf16", "rms", 0.1, 1e-6)
+
+    def call(rb, rc, acc=0, mask=FAKE, ptr=FAKE):
+        return L.sp_rs_dropout_residual_norm_bwd_rows(ctypes.byref(d), rb, rc, acc, ptr, ptr, ptr, ptr, mask,
+                                                      ptr, ptr, ptr, ptr, FAKE, FAKE, FAKE, 1 << 30, None)
+    for rb, rc in [(-1, 4), (0, -1), (17, 0), (10, 7), (1 << 62, 1 << 62)]:
+        assert call(rb, rc) == 1, (rb, rc)
+    assert call(16, 0, acc=1) == 0              # empty and accumulating: nothing launched
+    assert call(3, 0, acc=1, ptr=0) == 0        # ... and no per-row pointer needed
+    assert call(0, 4, ptr=0) == 1
+    assert call(1, 4) == 3                      # row 1's mask bytes start 24 bytes in
+    assert call(1, 4, mask=0) in (0, 6)         # regenerated mask: accepted (6 = no GPU)
+    assert call(2, 4) in (0, 6)
 
 
 @pytest.mark.parametrize("args,code", [

@@ -420,6 +420,95 @@ def test_bwd_parity(name, j, nshards, with_dh):
                orc_f["mask"], out)
 
 
+def _bwd_rows_chunks(w, d, cuts, dy, dh, saved, gamma, ws):
+    """The backward run chunk by chunk over row ranges, dgamma/dbeta
+    accumulated: sentinel-filled outputs, garbage in dgamma/dbeta before the
+    first chunk (which must replace it)."""
+    rows, H = dy.shape
+    out = dict(d_res=torch.full_like(dy, -3.0), d_sum=torch.full_like(dy, -3.0),
+               dgamma=torch.full((H,), 1e30, device=DEV), dbeta=torch.full((H,), 1e30, device=DEV)
+               if w.norm == "ln" else None)
+    for c, (b, e) in enumerate(zip(cuts[:-1], cuts[1:])):
+        ops.sp_rs_dropout_residual_norm_bwd_rows(d, b, e - b, c > 0, dy, dh, saved["h"], gamma, saved["mask"],
+                                                 saved["rstd"], saved["mean"] if w.norm == "ln" else None,
+                                                 out["d_res"], out["d_sum"], out["dgamma"], out["dbeta"], ws)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("name,j,nshards,cuts", [
+    ("pages_rms_bf16", 0, 2, [0, 1, 1000, 2049, 4096]),
+    ("gpt_ln_bf16", 3, 1, [0, 129, 130, 512]),
+    ("tiny_rms_f32", 1, 1, [0, 3, 11, 16]),
+])
+def test_bwd_rows_chunks_accumulate_to_the_full_call(name, j, nshards, cuts):
+    """The backward chunk by chunk over row ranges (each chunk's d_sum ready
+    for its all-gather while the next one computes): d_residual and d_sum bit
+    for bit the full call's; dgamma/dbeta, accumulated over the chunks in
+    order, equal the full call's up to the grouping of the sum, and the same
+    from run to run."""
+    w = syn.WORKLOADS[name]
+    inp = syn.fwd_inputs(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    pr, orc_f, saved, dy, dh = _bwd_inputs_from_oracle_fwd(w, j, nshards, inp, grads)
+    d = _desc(w, j, nshards)
+    ws = ops.workspace_for(d, DEV)
+    ref = ops.backward(d, dy, dh, saved["h"], inp["gamma"], saved["mask"], saved["rstd"],
+                       saved["mean"] if w.norm == "ln" else None, ws)
+    torch.cuda.synchronize()
+    one = _bwd_rows_chunks(w, d, cuts, dy, dh, saved, inp["gamma"], ws)
+    two = _bwd_rows_chunks(w, d, cuts, dy, dh, saved, inp["gamma"], ws)
+    for k in ("d_res", "d_sum"):
+        assert torch.equal(one[k], ref[k]), k
+    for k in ("dgamma", "dbeta"):
+        if ref[k] is None:
+            continue
+        assert torch.equal(one[k], two[k]), k
+        scale = ref[k].abs().max().item()
+        assert (one[k] - ref[k]).abs().max().item() <= 1e-5 * scale, k
+    _check_bwd(w, pr, orc_f["h"], _np(dy), _np(dh), _np(inp["gamma"]), orc_f["mask"], one)
+
+
+def test_pipelined_exchange_on_one_nccl_rank():
+    """forward_pipelined and backward_pipelined through NCCL on a one-rank
+    group (T = 1): the chunked kernels are ordered with the collectives on the
+    current stream and reproduce the whole-shard calls."""
+    import socket
+    import torch.distributed as dist
+    from residual_sp_rs_gb300 import sp_exchange as ex
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        w = syn.WORKLOADS["pages_rms_bf16"].with_(T=1, S=1024, B=2)
+        inp = syn.fwd_inputs(w, DEV)
+        grads = syn.upstream_grads(w, DEV)
+        d = _desc(w, 0)
+        ref = _gpu_fwd(w, inp, 0)
+        out = _sentinel_like(ref)
+        ex.forward_pipelined(d, inp["partials"][0], inp["residual"].view(-1, w.H), inp["gamma"], None,
+                             out["h"], out["y"], out["mask"], out["rstd"], None, chunks=4)
+        torch.cuda.synchronize()
+        for k in out:
+            assert torch.equal(out[k], ref[k]), k
+        ws = ops.workspace_for(d, DEV)
+        dy, dh = grads["dy"].view(-1, w.H), grads["dh_out"].view(-1, w.H)
+        bref = ops.backward(d, dy, dh, ref["h"], inp["gamma"], ref["mask"], ref["rstd"], None, ws)
+        d_res, d_sum = torch.empty_like(dy), torch.empty_like(dy)
+        dgamma = torch.empty(w.H, device=DEV)
+        grad, works = ex.backward_pipelined(d, dy, dh, ref["h"], inp["gamma"], ref["mask"], ref["rstd"], None,
+                                            d_res, d_sum, dgamma, None, ws, chunks=4)
+        for wk in works:
+            wk.wait()
+        torch.cuda.synchronize()
+        assert torch.equal(d_res, bref["d_res"]) and torch.equal(d_sum, bref["d_sum"])
+        assert torch.equal(grad, bref["d_sum"])       # one rank: the gather is its own shard
+        assert (dgamma - bref["dgamma"]).abs().max().item() <= 1e-5 * bref["dgamma"].abs().max().item()
+    finally:
+        dist.destroy_process_group()
+
+
 def test_bwd_gpt_layernorm_every_shard():
     """GPT-style LayerNorm (T=8, 512 token rows per shard): the backward of
     each single shard j = 0..7, with dgamma/dbeta over that shard's rows."""

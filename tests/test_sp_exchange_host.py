@@ -173,3 +173,41 @@ def test_chunk_bounds_keep_mask_rows_aligned():
                 assert all(e > s and (s * H) % 16 == 0 for s, e in b)
     with pytest.raises(ValueError):
         ex.chunk_bounds(4, 8, 0)
+
+
+def _gather_rank(rank, world, port, q, R, H, chunks):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from residual_sp_rs_gb300 import sp_exchange as ex
+    d_sum = (1000.0 * rank + torch.arange(R, dtype=torch.float64)[:, None]) * torch.ones(R, H, dtype=torch.float64)
+    grad = torch.full((world * R, H), float("nan"), dtype=torch.float64)
+    works = [ex.post_chunk_gather(d_sum, grad, R, b, e) for b, e in ex.chunk_bounds(R, H, chunks)]
+    for w in works:
+        w.wait()
+    whole = ex.gather_partial_grads(d_sum)
+    q.put((rank, grad.numpy(), whole.numpy()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,chunks", [(2, 3), (4, 4)])
+def test_chunked_gather_assembles_the_partials_gradient(world, chunks):
+    """The backward of the reduce-scatter gathered chunk by chunk, as the
+    pipelined backward posts it, equals the whole shard's all-gather."""
+    R, H = 10, 8
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_gather_rank, args=(r, world, port, q, R, H, chunks)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=180) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    expect = np.repeat(1000.0 * np.arange(world), R)[:, None] + np.tile(np.arange(R, dtype=np.float64), world)[:, None]
+    for _, grad, whole in got:
+        assert np.array_equal(grad, whole)
+        assert np.array_equal(grad, expect * np.ones(H))
