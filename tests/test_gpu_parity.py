@@ -239,6 +239,22 @@ def test_fwd_rows_chunks_equal_the_full_call(name, j, nshards, cuts):
         assert torch.equal(out[k], ref[k]), k
 
 
+def test_fwd_rows_chunks_without_mask_equal_the_full_call():
+    """Row ranges with no stored mask: the keep decisions come from the
+    global element index, so h and y match the full call's bit for bit."""
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    d = _desc(w, 0, 2)
+    ref = _gpu_fwd(w, inp, 0, 2)
+    out = _sentinel_like(ref)
+    out["mask"] = None
+    for b, e in zip([0, 777, 2048], [777, 2048, 4096]):
+        _fwd_rows_call(w, inp, d, 0, b, e - b, out)
+    torch.cuda.synchronize()
+    for k in ("h", "y", "rstd"):
+        assert torch.equal(out[k], ref[k]), k
+
+
 def test_fwd_rows_writes_only_its_range():
     w = syn.WORKLOADS["pages_rms_bf16"]
     inp = syn.fwd_inputs(w, DEV)
@@ -467,6 +483,25 @@ def test_bwd_rows_chunks_accumulate_to_the_full_call(name, j, nshards, cuts):
         scale = ref[k].abs().max().item()
         assert (one[k] - ref[k]).abs().max().item() <= 1e-5 * scale, k
     _check_bwd(w, pr, orc_f["h"], _np(dy), _np(dh), _np(inp["gamma"]), orc_f["mask"], one)
+
+
+def test_bwd_rows_chunks_regenerate_the_mask_of_their_rows():
+    """Row ranges of the mask-free backward: each range draws the keep bits of
+    its own global rows, so d_residual and d_sum match the full call's (which
+    reads the stored mask) bit for bit."""
+    w = syn.WORKLOADS["pages_rms_bf16"]
+    inp = syn.fwd_inputs(w, DEV)
+    grads = syn.upstream_grads(w, DEV)
+    pr, orc_f, saved, dy, dh = _bwd_inputs_from_oracle_fwd(w, 0, 2, inp, grads)
+    d = _desc(w, 0, 2)
+    ws = ops.workspace_for(d, DEV)
+    ref = ops.backward(d, dy, dh, saved["h"], inp["gamma"], saved["mask"], saved["rstd"], None, ws)
+    torch.cuda.synchronize()
+    free = dict(saved, mask=None)
+    one = _bwd_rows_chunks(w, d, [0, 333, 2049, 4096], dy, dh, free, inp["gamma"], ws)
+    for k in ("d_res", "d_sum"):
+        assert torch.equal(one[k], ref[k]), k
+    assert (one["dgamma"] - ref["dgamma"]).abs().max().item() <= 1e-5 * ref["dgamma"].abs().max().item()
 
 
 def test_pipelined_exchange_on_one_nccl_rank():
