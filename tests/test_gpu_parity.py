@@ -164,6 +164,8 @@ def test_fwd_edge_shapes(case):
     for j in sorted({0, T - 1}):
         _full_fwd_check(w, inp, j)
     _full_fwd_check(w, inp, 0, nshards=T)
+    if T >= 3:   # a run of shards from the middle of the group
+        _full_fwd_check(w, inp, 1, nshards=T - 2)
 
 
 def test_fwd_p0_without_mask_is_exact_residual_add():
@@ -181,6 +183,15 @@ def test_fwd_p0_without_mask_is_exact_residual_add():
     g["mask"] = np.ones_like(orc["mask"])
     g["mean"] = np.zeros(R)
     parity.compare_fwd("bf16", "rms", g, orc, pr, _np(inp["gamma"]))
+
+
+@pytest.mark.parametrize("name,j,nshards", [("gpt_ln_bf16", 2, 3), ("gpt_ln_bf16", 5, 3)])
+def test_fwd_run_of_middle_shards(name, j, nshards):
+    """Shards j .. j+nshards-1 from the middle of the group in one call: the
+    global row offset j*R keys the partial rows and the mask."""
+    w = syn.WORKLOADS[name]
+    inp = syn.fwd_inputs(w, DEV)
+    _full_fwd_check(w, inp, j, nshards)
 
 
 def test_fwd_from_shard_rows_equals_full_tensor_call():
@@ -421,7 +432,8 @@ def _check_bwd(w, pr, saved_np, dy_np, dh_np, gamma_np, mask_np, gout):
 
 @pytest.mark.parametrize("name,j,nshards", [("tiny_rms_f32", 0, 1), ("tiny_rms_f32", 1, 1),
                                             ("pages_rms_bf16", 0, 1), ("pages_rms_bf16", 0, 2),
-                                            ("gpt_ln_bf16", 3, 1), ("gpt_ln_bf16", 0, 8)])
+                                            ("gpt_ln_bf16", 3, 1), ("gpt_ln_bf16", 0, 8),
+                                            ("gpt_ln_bf16", 2, 3)])   # a run of shards from the middle
 @pytest.mark.parametrize("with_dh", [True, False])
 def test_bwd_parity(name, j, nshards, with_dh):
     w = syn.WORKLOADS[name]
