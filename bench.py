@@ -433,9 +433,57 @@ def measure_workload(w, dev, hbm_peak, cpu_seconds=None):
                           "sp2hp": _kernel_entry(t_sp2hp, layout_bytes(w, rows), hbm_peak)}}
     del hn, g
     torch.cuda.empty_cache()
+    # the same bytes moved by a pure copy in one launch, for scale
+    for k in ("fwd", "bwd"):
+        e = out["per_kernel"][k]
+        cf = measure_copy_floor(dev, e["algorithmic_bytes"], w.H, hbm_peak)
+        e["copy_at_same_bytes_gbs"] = cf["gbs"]
+        e["frac_of_copy_at_same_bytes"] = round(e["gbs"] / cf["gbs"], 4)
     if cpu_seconds:
         out["cpu_baseline"] = cpu_baseline(w, cpu_seconds)
     return out
+
+
+def measure_copy_floor(dev, nbytes, H, hbm_peak):
+    """sp2hp, a pure copy (each byte read once and written once), of about
+    `nbytes` read plus written bytes in rows of H bf16 elements, back to back
+    over sets rotating past the L2: what moving that many bytes in one launch
+    costs on this GPU, launch and ramp included."""
+    import torch
+
+    from residual_sp_rs_gb300 import ops
+
+    T = 2
+    N = max(T, int(nbytes // (4 * H)) // T * T)
+    byt = 4 * N * H
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(2, -(-2 * l2 // byt) + 1)
+    gen = torch.Generator(device=dev).manual_seed(4242)
+    xs = [torch.randn((N, H), device=dev, generator=gen).to(torch.bfloat16) for _ in range(n_sets)]
+    ys = [torch.empty((T, N, H // T), device=dev, dtype=torch.bfloat16) for _ in xs]
+    cap = torch.cuda.Stream()
+    for k in range(n_sets):
+        ops.sp2hp(xs[k], ys[k], N, H, T, 1)
+    per_graph = max(16, n_sets)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+        for i in range(per_graph):
+            ops.sp2hp(xs[i % n_sets], ys[i % n_sets], N, H, T, 1)
+    g.replay()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(21)]
+    evs[0].record()
+    for i in range(20):
+        g.replay()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    ms = float(np.median([evs[i].elapsed_time(evs[i + 1]) for i in range(20)])) / per_graph
+    del xs, ys, g
+    torch.cuda.empty_cache()
+    d = _kernel_entry(ms, byt, hbm_peak)
+    d["note"] = (f"sp_layout_kernel (sp2hp, a pure copy) of {byt} read+written bytes, N={N} H={H}, "
+                 f"{n_sets} buffer sets, back to back: the cost of moving that many bytes in one launch")
+    return d
 
 
 def measure_layout(dev, hbm_peak):
@@ -626,6 +674,10 @@ def run_ours(args):
                                  "of 50 launches each alone between events and a synchronize "
                                  "(includes launch latency)",
                 "per_kernel": {k: _kernel_entry(v[0], v[1], hbm_peak, single[k]) for k, v in kern.items()}}
+    if world == 1 and not args.seq:
+        cf = measure_copy_floor(dev, d_bytes, H, hbm_peak)
+        roofline["copy_at_same_bytes"] = cf
+        roofline["frac_of_copy_at_same_bytes"] = round(achieved / cf["gbs"], 4)
 
     # ---- end to end: pinned host inputs in, results out, every step -------------
     e2e = None
