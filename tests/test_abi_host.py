@@ -228,3 +228,51 @@ def test_product_package_does_not_import_oracle():
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, f
                 assert "oracle.h" not in txt and "liboracle" not in txt, f
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "spfuse.h"
+
+int main(void) {
+  sp_rs_desc_t d;
+  sp_plan_info_t info;
+  memset(&d, 0, sizeof d);
+  d.T = 2; d.j = 0; d.S = 2048; d.B = 2; d.H = 768;
+  d.dtype = SP_BF16; d.norm = SP_RMSNORM; d.p = 0.1f; d.eps = 1e-6f; d.seed = 0; d.nshards = 2;
+  if (sp_plan_describe(&d, 152, 232448, 1, 1, &info) != SP_OK) return 1;
+  printf("version %d fwd_block %d bwd_block %d bwd_ws %lld\n", (int)sp_version(), (int)info.fwd.block,
+         (int)info.bwd.block, (long long)info.bwd.workspace_bytes);
+  d.T = 0;  /* invalid: refused before anything touches a device */
+  printf("invalid %d %s\n", (int)sp_rs_dropout_residual_norm_fwd(&d, NULL, NULL, NULL, NULL, NULL, NULL,
+                                                                  NULL, NULL, NULL, NULL),
+         sp_status_string(SP_ERR_INVALID_ARG));
+  printf("workspace %lu\n", (unsigned long)sp_rs_bwd_workspace_bytes(&d));
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(spf, tmp_path):
+    """The boundary is a C ABI: a C11 program compiled with warnings as errors
+    includes the header, links libspfuse and calls entry points that need no
+    GPU (launch plans, validation, status strings)."""
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(spf.LIB_PATH)
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{os.path.join(ROOT, 'include')}",
+                        str(src), "-o", str(exe), f"-L{libdir}", "-l:" + os.path.basename(spf.LIB_PATH),
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    lines = out.stdout.split("\n")
+    assert lines[0].startswith("version ") and "fwd_block 896" in lines[0] and "bwd_block 512" in lines[0]
+    assert lines[1].startswith("invalid 1 SP_ERR_INVALID_ARG")
+    assert lines[2] == "workspace 0"
